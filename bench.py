@@ -1,0 +1,489 @@
+"""Benchmark of the NVFP4 decode-step weight stream on GB300.
+
+Workload (default): the ~31B-shaped decoder stack, 60 layers x {fused QKV
+[8192, 5376], o_proj [5376, 4096], fused gate+up [43008, 5376], down
+[5376, 21504]} in NVFP4 (13,934,592,000 bytes of weights, far larger than
+L2), one bf16 token per projection, all 240 projections streamed in order on
+one stream per step through aq_decode_step_weights (captured once in a CUDA
+graph, programmatic dependent launch between projections).  Weights are
+seeded synthetic N(0, 0.02^2) with 0.1% x20 outliers, quantised on the GPU
+by the library before timing.
+
+Metric: algorithmic HBM GB/s of the step (0.5625 B per weight element + 4 B
+per-tensor scale + activations in + outputs out) and ms per step.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl aq|reference]
+
+One JSON line is printed by rank 0.  With N > 1 (torchrun) every rank runs
+an independent replica on its own GPU (the path has no exchange step).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "NVFP4 decode GEMV HBM GB/s (% of 8 TB/s); ms per 31B-shaped step weight stream"
+NOMINAL_HBM_GBS = 8000.0  # the 8 TB/s denominator the metric names
+
+# DRAM bytes per GEMV launch from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by the sha1 of the kernel source it was
+# taken on; when gemv.cu changes the figure no longer applies (null).
+NCU_TRAFFIC = {}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("aq", "reference"), default="aq")
+    p.add_argument("--m", type=int, default=1, help="tokens per projection")
+    p.add_argument("--workload", choices=("31b", "1b"), default="31b")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the eager / no-PDL / end-to-end / CPU-baseline legs")
+    return p.parse_args()
+
+
+def workload(name):
+    from nvfp4_block_scaled_aq_gb300 import inputs
+    if name == "31b":
+        return "gemma4-31b-shaped decode-step weight stream", inputs.LAYER_31B, inputs.LAYERS_31B
+    return "gemma3-1b-shaped decode-step weight stream", inputs.LAYER_1B, inputs.LAYERS_1B
+
+
+def algorithmic_bytes(shapes, layers, m):
+    """Bytes one step must move at minimum: NVFP4 weights (packed nibbles +
+    one E4M3 scale per 16 elements = 0.5625 B/element), the fp32 per-tensor
+    scale, the bf16 activations read and the bf16 outputs written."""
+    per_layer = 0
+    for n, k in shapes:
+        per_layer += n * k // 2 + n * k // 16 + 4 + 2 * m * k + 2 * m * n
+    return per_layer * layers
+
+
+def weight_bytes(shapes, layers):
+    return sum(n * k // 2 + n * k // 16 for n, k in shapes) * layers
+
+
+# ------------------------------------------------------------ distributed
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if self._cuda() else "gloo"
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    @staticmethod
+    def _cuda():
+        import torch
+        return torch.cuda.is_available()
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v):
+        if not self.pg:
+            return v
+        import torch
+        t = torch.tensor([v], dtype=torch.float64,
+                         device="cuda" if self._cuda() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.samples = []
+        self.error = None
+        self.proc = None
+        self.t0 = self.t1 = None
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        sel = self._selector(device_index)
+        if sel:
+            cmd += ["-i", sel]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError as e:
+            self.error = str(e)
+
+    @staticmethod
+    def _selector(idx):
+        try:
+            import torch
+            u = str(torch.cuda.get_device_properties(idx).uuid)
+            return u if u.startswith("GPU-") else "GPU-" + u
+        except Exception:
+            return None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.samples.append((time.time(), parts))
+
+    def window(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "note": self.error or "no nvidia-smi samples"}
+        inside = [p for t, p in self.samples
+                  if self.t0 is None or (self.t0 - 0.1 <= t <= self.t1 + 0.1)]
+        if not inside:  # timed region shorter than the sampling period
+            mid = 0.5 * (self.t0 + self.t1)
+            inside = [min(self.samples, key=lambda s: abs(s[0] - mid))[1]]
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[0]) for p in inside if num(p[0]) is not None]
+        mx = [num(p[1]) for p in inside if num(p[1]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({nm for p in inside for nm, v in zip(names, p[4:8])
+                          if v.strip().lower() == "active"})
+        pw = [num(p[2]) for p in inside if num(p[2]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "power_w_max": max(pw) if pw else None}
+
+
+# ------------------------------------------------------------ the aq arm
+
+class Stack:
+    """All projections of the workload resident in HBM, plus one
+    activation buffer and one output buffer sliced per projection."""
+
+    def __init__(self, shapes, layers, m, device, seed=0):
+        import torch
+        from nvfp4_block_scaled_aq_gb300 import aq, inputs
+        self.shapes, self.layers, self.m = shapes, layers, m
+        qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+        self.weights = []
+        for layer in range(layers):
+            for p, (n, k) in enumerate(shapes):
+                W = inputs.weight(n, k, seed=inputs.seed_of(seed, layer, p), device=device)
+                w = aq.Nvfp4Weight.empty(n, k, device=device)
+                aq.quantize(W, w, qws)
+                del W
+                self.weights.append(w)
+        x_elems = [m * k for _ in range(layers) for (n, k) in shapes]
+        y_elems = [m * n for _ in range(layers) for (n, k) in shapes]
+        self.x_all = torch.empty(sum(x_elems), dtype=torch.bfloat16, device=device)
+        self.y_all = torch.empty(sum(y_elems), dtype=torch.bfloat16, device=device)
+        self.xs, self.ys = [], []
+        xo = yo = 0
+        for i, (xe, ye) in enumerate(zip(x_elems, y_elems)):
+            n, k = shapes[i % len(shapes)]
+            self.xs.append(self.x_all[xo:xo + xe].view(m, k))
+            self.ys.append(self.y_all[yo:yo + ye].view(m, n))
+            xo += xe
+            yo += ye
+        for i, x in enumerate(self.xs):
+            layer, p = divmod(i, len(shapes))
+            x.copy_(inputs.tokens(m, x.shape[1], seed=inputs.seed_of(seed + 1, layer, p),
+                                  device=device))
+        ws_bytes = max(aq.gemv_workspace_bytes(n, k, m) for n, k in shapes)
+        self.ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=device)
+        self.args = aq.StepArgs(self.weights, self.xs, self.ys)
+        torch.cuda.synchronize()
+        st = aq.poll_device_status()
+        if st != aq.OK:
+            raise RuntimeError("quantisation reported %s: %s" % (st, aq.last_error()))
+
+    @property
+    def launches(self):
+        return len(self.weights)
+
+
+def capture(stack, flags, stream):
+    import torch
+    from nvfp4_block_scaled_aq_gb300 import aq
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        aq.decode_step(stack.args, stack.ws, flags=flags, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            aq.decode_step(stack.args, stack.ws, flags=flags, stream=stream)
+    torch.cuda.synchronize()
+    return g
+
+
+def time_region(run_step, steps, warmup, stream, dist, sampler=None):
+    """Seconds for `steps` steps: barrier + synchronize on both sides, CUDA
+    events recorded on the launching stream; max over ranks."""
+    import torch
+    for _ in range(warmup):
+        run_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    e0.record(stream)
+    for _ in range(steps):
+        run_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.time()
+    dist.barrier()
+    if sampler:
+        sampler.window(t0, t1)
+    return dist.max(e0.elapsed_time(e1) / 1e3)
+
+
+def kernel_sha():
+    src = os.path.join(ROOT, "nvfp4_block_scaled_aq_gb300", "csrc", "gemv.cu")
+    return hashlib.sha1(open(src, "rb").read()).hexdigest()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def cpu_baseline(shapes, m, budget_s=12.0, seed=0):
+    """The oracle's fp64 GEMV, as it stands, on the host: rows of layer 0's
+    projections (seeded like the GPU workload but drawn on the CPU) until
+    the time budget is spent.  Returns GB/s of algorithmic bytes."""
+    import numpy as np
+    import oracle
+    from nvfp4_block_scaled_aq_gb300 import inputs
+    done_bytes = 0.0
+    spent = 0.0
+    rows_done = 0
+    per_proj = budget_s / len(shapes)
+    for p, (n, k) in enumerate(shapes):
+        rows = min(n, 1024)
+        W = inputs.bits_u16(inputs.weight(rows, k, seed=inputs.seed_of(seed, 0, p)))
+        x = inputs.bits_u16(inputs.tokens(m, k, seed=inputs.seed_of(seed + 1, 0, p)))
+        packed, scales, ge, gd = oracle.quantize(W)
+        r0 = 0
+        t_proj = 0.0
+        while r0 < rows and t_proj < per_proj:
+            r1 = min(rows, r0 + 64)
+            sel = np.arange(r0, r1)
+            t = time.perf_counter()
+            oracle.gemv(packed, scales, gd, x, rows=sel)
+            dt = time.perf_counter() - t
+            t_proj += dt
+            done_bytes += (r1 - r0) * (k // 2 + k // 16) + 2 * m * (r1 - r0)
+            rows_done += r1 - r0
+            r0 = r1
+        done_bytes += 2 * m * k + 4
+        spent += t_proj
+    return {"value": done_bytes / spent / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d rows of layer-0 projections (of %d rows x 60 layers), m=%d, "
+                      "fp64 accumulation, single thread" % (rows_done, sum(n for n, _ in shapes), m),
+            "seconds": round(spent, 3)}
+
+
+def run_aq(a, dist):
+    import torch
+    from nvfp4_block_scaled_aq_gb300 import aq
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(dist.local)
+    device = torch.device("cuda", dist.local)
+    name, shapes, layers = workload(a.workload)
+    stack = Stack(shapes, layers, a.m, device)
+    step_bytes = algorithmic_bytes(shapes, layers, a.m)
+    stream = torch.cuda.Stream(device)
+
+    g_pdl = capture(stack, aq.STEP_PDL, stream)
+    sampler = ClockSampler(dist.local) if dist.rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    secs = time_region(g_pdl.replay, a.steps, a.warmup, stream, dist, sampler)
+    if sampler:
+        sampler.stop()
+    ms = secs / a.steps * 1e3
+    value = dist.world * step_bytes * a.steps / secs / 1e9
+
+    extras = {}
+    e2e = None
+    if not a.no_extras:
+        g_nopdl = capture(stack, 0, stream)
+        extras["graph_no_pdl_ms_per_step"] = round(
+            time_region(g_nopdl.replay, a.steps, a.warmup, stream, dist) / a.steps * 1e3, 4)
+        del g_nopdl
+
+        def eager():
+            aq.decode_step(stack.args, stack.ws, flags=aq.STEP_PDL, stream=stream)
+        with torch.cuda.stream(stream):
+            extras["eager_pdl_ms_per_step"] = round(
+                time_region(eager, a.steps, a.warmup, stream, dist) / a.steps * 1e3, 4)
+
+        # end to end through the C ABI: pinned host activations in, outputs out
+        x_host = torch.empty(stack.x_all.numel(), dtype=torch.bfloat16, pin_memory=True)
+        x_host.copy_(stack.x_all)
+        y_host = torch.empty(stack.y_all.numel(), dtype=torch.bfloat16, pin_memory=True)
+
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                stack.x_all.copy_(x_host, non_blocking=True)
+                aq.decode_step(stack.args, stack.ws, flags=aq.STEP_PDL, stream=stream)
+                y_host.copy_(stack.y_all, non_blocking=True)
+        e2e_secs = time_region(e2e_step, a.steps, a.warmup, stream, dist)
+        e2e = {"value": round(dist.world * step_bytes * a.steps / e2e_secs / 1e9, 2),
+               "unit": "GB/s",
+               "ms_per_step": round(e2e_secs / a.steps * 1e3, 4),
+               "h2d_bytes_per_step": stack.x_all.numel() * 2,
+               "d2h_bytes_per_step": stack.y_all.numel() * 2,
+               "path": "aq_decode_step_weights, eager launches, pinned host buffers"}
+
+    st = aq.poll_device_status()
+    if st != aq.OK:
+        raise RuntimeError("device status %d after timing: %s" % (st, aq.last_error()))
+
+    peak, peak_kind = load_peaks()
+    launch_bytes = step_bytes / stack.launches
+    launch_s = secs / a.steps / stack.launches
+    achieved = launch_bytes / launch_s / 1e9
+    traffic = NCU_TRAFFIC.get(kernel_sha())
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)",
+                "kernel": "gemv_kernel<1> (aq_gemv_nvfp4 / aq_decode_step_weights)",
+                "algorithmic_bytes_per_launch": round(launch_bytes)}
+
+    cpu = None
+    if dist.rank == 0 and not a.no_extras:
+        cpu = cpu_baseline(shapes, a.m)
+
+    clocks = sampler.summary() if sampler else None
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s",
+        "n_gpus": dist.world, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 weights, bf16 activations, fp32 accumulate",
+        "data": "synthetic (seeded N(0,0.02^2) weights with 0.1% x20 outliers, N(0,1) tokens)",
+        "pct_of_8tbs": round(100.0 * value / dist.world / NOMINAL_HBM_GBS, 2),
+        "config": {"workload": name, "layers": layers,
+                   "projections": [list(s) for s in shapes], "m": a.m,
+                   "weight_bytes_per_step": weight_bytes(shapes, layers),
+                   "algorithmic_bytes_per_step": step_bytes,
+                   "graph": True, "pdl": True,
+                   "l2": "inputs larger than L2 (weights %.1f GB per step)" %
+                         (weight_bytes(shapes, layers) / 1e9),
+                   "parallelism": "replicas x%d" % dist.world},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": stack.launches * a.steps,
+        "clocks": clocks,
+        "extras": extras,
+    }
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(a, dist):
+    """The CPU oracle as it stands, on the host cores, on a bounded sample
+    of the same workload: each step is the oracle's GEMV over 256 rows of
+    each of layer 0's projections."""
+    if dist.rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from nvfp4_block_scaled_aq_gb300 import inputs
+    name, shapes, layers = workload(a.workload)
+    m = a.m
+    prepared = []
+    for p, (n, k) in enumerate(shapes):
+        rows = min(n, 64)
+        W = inputs.bits_u16(inputs.weight(rows, k, seed=inputs.seed_of(0, 0, p)))
+        x = inputs.bits_u16(inputs.tokens(m, k, seed=inputs.seed_of(1, 0, p)))
+        packed, scales, ge, gd = oracle.quantize(W)
+        prepared.append((packed, scales, gd, x, rows, k))
+    step_bytes = sum(r * (k // 2 + k // 16) + 2 * m * k + 2 * m * r + 4
+                     for _, _, _, _, r, k in prepared)
+
+    def step():
+        for packed, scales, gd, x, rows, k in prepared:
+            oracle.gemv(packed, scales, gd, x)
+    for _ in range(a.warmup):
+        step()
+    t = time.perf_counter()
+    for _ in range(a.steps):
+        step()
+    secs = time.perf_counter() - t
+    value = step_bytes * a.steps / secs / 1e9
+    sample = ("64 rows of each of layer 0's 4 projections per step (%d of %d weight bytes "
+              "of a full step), m=%d, fp64 accumulation" %
+              (sum(r * (k // 2 + k // 16) for _, _, _, _, r, k in prepared),
+               weight_bytes(shapes, layers), m))
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+           "n_gpus": dist.world, "steps": a.steps, "warmup": a.warmup,
+           "ms_per_step": round(secs / a.steps * 1e3, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate (CPU oracle)",
+           "data": "synthetic (seeded, drawn on the CPU)",
+           "config": {"workload": name + " (bounded sample)", "m": m},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                            "kind": "oracle", "sample": sample},
+           "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    a = parse()
+    dist = Dist()
+    try:
+        if a.impl == "reference":
+            run_reference(a, dist)
+        else:
+            run_aq(a, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

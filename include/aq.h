@@ -1,0 +1,210 @@
+/*
+ * aq.h -- C ABI of the NVFP4 decode-projection library (libaq.so) for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (sources are the AttnQuant / Weightless
+ * documentation pages; page title, then section):
+ *   - the effective weight of a theta bundle, W_eff = s*W0 + U*V^T, rebuilt
+ *     once at load ("AttnQuant" landing page, "How it works"; Weightless
+ *     "GPU and cache acceleration", "Precompute-outside (the fast path)");
+ *   - its round-to-nearest NVFP4 quantisation: packed E2M1 nibbles, one
+ *     E4M3 scale per 16 elements along K, one fp32 per-tensor scale
+ *     (landing page "Results"; "GPU acceleration", "NVFP4 quantization";
+ *     "Throughput", "What quantization actually saves");
+ *   - the batch-1 / small-batch decode product y = x * W_hat^T streamed
+ *     once per token, with Q/K/V and gate/up fused into single weights
+ *     ("GPU acceleration", "Q/K/V fusion"; Weightless "Future work": a GEMV
+ *     that dequantises in registers and streams at full HBM bandwidth);
+ *   - the per-step stream of all projections of a decoder, one launch per
+ *     fused projection ("GPU acceleration", "CUDA graph capture").
+ *
+ * Conventions shared by every entry point:
+ *   - bf16 values are passed as uint16_t bit patterns.
+ *   - Every pointer argument is DEVICE memory owned by the caller unless
+ *     the comment says "host".  The library never allocates and never
+ *     frees; it keeps no pointer after a call returns.
+ *   - All work is asynchronous on the given stream (NULL = legacy default
+ *     stream).  No call synchronises except aq_poll_device_status.
+ *   - Arguments are validated on the host before any launch; a failed
+ *     check launches nothing and returns an error code, with a message in
+ *     aq_last_error().  Conditions only the device can see (a non-finite
+ *     per-tensor amax, a bounded wait that gave up) are recorded in a
+ *     device status word that aq_poll_device_status() reads and clears.
+ *   - No C++ exception crosses this interface.
+ *   - The stream type is the CUDA runtime's cudaStream_t (struct
+ *     CUstream_st *); it is spelled here so the header needs no CUDA
+ *     include.
+ */
+#ifndef AQ_H
+#define AQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Only the entry points below are exported from libaq.so. */
+#if defined(__GNUC__)
+#define AQ_API __attribute__((visibility("default")))
+#else
+#define AQ_API
+#endif
+
+typedef struct CUstream_st *aq_stream_t;
+
+typedef enum {
+  AQ_OK = 0,
+  AQ_ERR_INVALID_ARG = 1, /* null pointer, unknown enum value            */
+  AQ_ERR_SHAPE = 2,       /* n, k, m or r outside the supported range     */
+  AQ_ERR_ALIGNMENT = 3,   /* a pointer misses its stated alignment        */
+  AQ_ERR_RANGE = 4,       /* per-tensor amax non-finite or too small      */
+  AQ_ERR_UNSUPPORTED = 5, /* no sm_103 device, or path not available      */
+  AQ_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up           */
+  AQ_ERR_CUDA = 7,        /* a CUDA runtime call failed                   */
+  AQ_ERR_WORKSPACE = 8    /* workspace missing, too small or misaligned   */
+} aq_status;
+
+/* An NVFP4 weight of shape [n, k] (n output rows, k input columns).  The
+ * struct itself lives in host memory; its pointers are device memory.
+ *   packed        n * k / 2 bytes, row-major; byte i of a row holds
+ *                 element 2i in its low nibble and 2i+1 in its high
+ *                 nibble; 16-byte aligned.
+ *   scales        aq_scale_bytes(n, k) bytes of E4M3 block scales (one per
+ *                 16 elements along k) in the device tile layout: tiles of
+ *                 16 rows x 128 columns, tile (tn, tk) at byte
+ *                 (tn * ceil(k/128) + tk) * 128; inside a tile, row
+ *                 r = 8h + g and block j = 2c + p sit at byte
+ *                 (4g + c) * 4 + 2h + p; padding bytes are zero.  One
+ *                 32-bit word of a tile holds what one GEMV lane needs.
+ *                 16-byte aligned.
+ *   global_scale  one fp32: the per-tensor decode scale g_dec = amax/2688
+ *                 (1 for an all-zero tensor).
+ * A fused projection (Q/K/V, or gate and up) is one weight whose rows are
+ * the row-wise concatenation of its parts, quantised with one per-tensor
+ * scale. */
+typedef struct {
+  int32_t n;
+  int32_t k;
+  uint8_t *packed;
+  uint8_t *scales;
+  float *global_scale;
+} aq_nvfp4_weight;
+
+/* Shape limits: 1 <= n <= 2^24, 32 <= k <= 2^20, k % 32 == 0,
+ * 0 <= r <= 64, 1 <= m <= AQ_MAX_M for the GEMV path. */
+#define AQ_MAX_M 16
+
+/* Bytes of the packed nibbles and of the scale layout of an [n, k] weight.
+ * For n % 16 == 0 and k % 128 == 0 the two add up to 0.5625 * n * k.
+ * Return 0 for shapes outside the limits. */
+AQ_API size_t aq_packed_bytes(int32_t n, int32_t k);
+AQ_API size_t aq_scale_bytes(int32_t n, int32_t k);
+
+/* W_eff = bf16(s*W0 + U*V^T) ("How it works").  W0 [n, k], U [n, r],
+ * V [k, r] bf16 row-major; s fp32 [n]; W_eff [n, k] bf16.  Per element the
+ * rank-r term is summed first in fp32 (fused multiply-adds, r ascending,
+ * starting from +0); if it is zero the value is the fp32 product s*W0,
+ * otherwise one fused multiply-add s*W0 + delta; the fp32 result is rounded
+ * to bf16 (nearest, ties to even).  So s = 1, U = V = 0 returns W0
+ * bit-for-bit, -0 included.  r = 0 is allowed (U, V may then be NULL).
+ * W0 and W_eff: 16-byte aligned; W_eff may not overlap the inputs. */
+AQ_API aq_status aq_reconstruct(const uint16_t *W0, const float *s, const uint16_t *U,
+                         const uint16_t *V, int32_t n, int32_t k, int32_t r,
+                         uint16_t *W_eff, aq_stream_t stream);
+
+/* Workspace of aq_quantize_nvfp4 and aq_reconstruct_quantize_nvfp4: at
+ * least this many bytes, 256-byte aligned, device memory.  Its contents
+ * need no initialisation. */
+AQ_API size_t aq_quantize_workspace_bytes(void);
+
+/* Round-to-nearest NVFP4 quantisation of a bf16 weight W [n, k] into *out
+ * (whose n and k must equal the arguments).  Steps:
+ *   amax = max |W|; g_enc = 2688/amax, g_dec = amax/2688 (1 and 1 if
+ *   amax = 0); per 16-element block along k: b = max |w|,
+ *   sf = E4M3((b/6)*g_enc) rounded to nearest even and saturated at 448,
+ *   sd = decode(sf); if sd == 0 the block's nibbles are 0, else each
+ *   nibble is E2M1(w * (g_enc/sd)), nearest even, saturated at 6, with the
+ *   sign of the product kept even when the magnitude rounds to zero.
+ * Writes out->packed, out->scales and *out->global_scale.  A non-finite
+ * amax, or one so small that 2688/amax overflows, is caught on the device:
+ * the outputs are then zero-filled, *global_scale is NaN, and the next
+ * aq_poll_device_status() returns AQ_ERR_RANGE. */
+AQ_API aq_status aq_quantize_nvfp4(const uint16_t *W, int32_t n, int32_t k,
+                            const aq_nvfp4_weight *out, void *workspace,
+                            size_t workspace_bytes, aq_stream_t stream);
+
+/* The two steps above fused: W_eff is recomputed on the fly in both the
+ * amax pass and the quantisation pass and never written to memory.  The
+ * quantised bytes equal aq_reconstruct followed by aq_quantize_nvfp4. */
+AQ_API aq_status aq_reconstruct_quantize_nvfp4(const uint16_t *W0, const float *s,
+                                        const uint16_t *U, const uint16_t *V,
+                                        int32_t n, int32_t k, int32_t r,
+                                        const aq_nvfp4_weight *out,
+                                        void *workspace, size_t workspace_bytes,
+                                        aq_stream_t stream);
+
+/* GEMV paths. */
+typedef enum {
+  AQ_PATH_AUTO = 0, /* choose by m                                       */
+  AQ_PATH_GEMV = 1, /* bf16 activations, weight dequantised in registers */
+  AQ_PATH_MMA = 2   /* activations quantised to NVFP4, tcgen05 MMA       */
+} aq_path;
+
+/* Workspace of aq_gemv_nvfp4 / aq_decode_step_weights for a weight of
+ * shape [n, k] and m tokens: bytes, device memory, 256-byte aligned.  It
+ * must be ZERO-FILLED once after allocation; every call leaves it in the
+ * state it needs next, so one zeroed workspace serves any sequence of
+ * calls on one stream.  Calls that may run concurrently need separate
+ * workspaces. */
+AQ_API size_t aq_gemv_workspace_bytes(int32_t n, int32_t k, int32_t m);
+
+/* y[t, i] = bf16( sum_k x[t, k] * w_hat[i, k] ), w_hat = e2m1(q)*sd*g_dec,
+ * fp32 accumulation ("Future work": dequantise in registers).  x [m, k]
+ * bf16 and y [m, n] bf16 row-major, 16-byte aligned, y not overlapping x.
+ * The result does not depend on m (each token's output equals the m = 1
+ * call bit for bit) nor on timing: the split over the K axis is fixed by
+ * (n, k) and its partial sums are added in a fixed order. */
+AQ_API aq_status aq_gemv_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m,
+                        uint16_t *y, aq_path path, void *workspace,
+                        size_t workspace_bytes, aq_stream_t stream);
+
+/* Flags of aq_decode_step_weights. */
+#define AQ_STEP_PDL 1u /* programmatic dependent launch between projections */
+
+/* One decode step's weight stream: for p = 0 .. n_proj-1 in order,
+ * y[p] = GEMV(w[p], x[p]) with m tokens, all on one stream, one launch per
+ * projection.  w, x and y are HOST arrays of n_proj entries; the weights
+ * and activation buffers they point to are device memory.  Projection p+1
+ * reads its x only after projection p has completed (stream order, or with
+ * AQ_STEP_PDL a programmatic wait inside the kernel after it has started
+ * fetching its weights).  workspace must hold aq_gemv_workspace_bytes for
+ * the largest projection and be zero-filled once.  Safe to record into a
+ * CUDA graph. */
+AQ_API aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,
+                                 const uint16_t *const *x, uint16_t *const *y,
+                                 int32_t m, uint32_t flags, void *workspace,
+                                 size_t workspace_bytes, aq_stream_t stream);
+
+/* Test helper: the scales of w rewritten in canonical row-major order
+ * [n, k/16] into canon (device, n*k/16 bytes). */
+AQ_API aq_status aq_scales_to_canonical(const aq_nvfp4_weight *w, uint8_t *canon,
+                                 aq_stream_t stream);
+
+/* Synchronise `stream`, read the device status word of the current device
+ * and clear it.  Returns AQ_OK, AQ_ERR_RANGE or AQ_ERR_TIMEOUT (the first
+ * condition recorded since the last poll), or AQ_ERR_CUDA. */
+AQ_API aq_status aq_poll_device_status(aq_stream_t stream);
+
+/* Message of the last error returned on the calling host thread ("" if
+ * none).  The string stays valid until the thread's next failing call. */
+AQ_API const char *aq_last_error(void);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+AQ_API int32_t aq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AQ_H */

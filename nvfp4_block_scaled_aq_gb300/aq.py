@@ -1,0 +1,227 @@
+"""ctypes binding of libaq.so, the C-ABI declared in include/aq.h.
+
+Argument marshalling only: every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory (``data_ptr()``)
+and streams (``cuda_stream``); nothing here computes on tensor values.
+The library is loaded on first use and a missing build raises
+``AqLibraryMissing`` -- there is no fallback.
+"""
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libaq.so")
+
+# aq_status
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_SHAPE = 2
+ERR_ALIGNMENT = 3
+ERR_RANGE = 4
+ERR_UNSUPPORTED = 5
+ERR_TIMEOUT = 6
+ERR_CUDA = 7
+ERR_WORKSPACE = 8
+STATUS_NAMES = {0: "AQ_OK", 1: "AQ_ERR_INVALID_ARG", 2: "AQ_ERR_SHAPE",
+                3: "AQ_ERR_ALIGNMENT", 4: "AQ_ERR_RANGE", 5: "AQ_ERR_UNSUPPORTED",
+                6: "AQ_ERR_TIMEOUT", 7: "AQ_ERR_CUDA", 8: "AQ_ERR_WORKSPACE"}
+
+PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
+STEP_PDL = 1
+MAX_M = 16
+
+
+class AqLibraryMissing(RuntimeError):
+    pass
+
+
+class AqError(RuntimeError):
+    def __init__(self, status, message):
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, status), message))
+        self.status = status
+
+
+class Nvfp4WeightC(C.Structure):
+    _fields_ = [("n", C.c_int32), ("k", C.c_int32), ("packed", C.c_void_p),
+                ("scales", C.c_void_p), ("global_scale", C.c_void_p)]
+
+
+_lib = None
+_p = C.c_void_p
+_i32 = C.c_int32
+_sz = C.c_size_t
+
+
+def lib():
+    """The loaded library (raises AqLibraryMissing if it was never built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise AqLibraryMissing(
+                "libaq.so is not built; run nvfp4_block_scaled_aq_gb300/build.py "
+                "(or __graft_entry__.build())")
+        L = C.CDLL(LIB_PATH)
+        _declare(L)
+        _lib = L
+    return _lib
+
+
+def _declare(L):
+    W = C.POINTER(Nvfp4WeightC)
+    sigs = {
+        "aq_version": ([], _i32),
+        "aq_last_error": ([], C.c_char_p),
+        "aq_packed_bytes": ([_i32, _i32], _sz),
+        "aq_scale_bytes": ([_i32, _i32], _sz),
+        "aq_reconstruct": ([_p, _p, _p, _p, _i32, _i32, _i32, _p, _p], C.c_int),
+        "aq_quantize_workspace_bytes": ([], _sz),
+        "aq_quantize_nvfp4": ([_p, _i32, _i32, W, _p, _sz, _p], C.c_int),
+        "aq_reconstruct_quantize_nvfp4": ([_p, _p, _p, _p, _i32, _i32, _i32, W, _p,
+                                           _sz, _p], C.c_int),
+        "aq_gemv_workspace_bytes": ([_i32, _i32, _i32], _sz),
+        "aq_gemv_nvfp4": ([W, _p, _i32, _p, C.c_int, _p, _sz, _p], C.c_int),
+        "aq_decode_step_weights": ([W, _i32, C.POINTER(_p), C.POINTER(_p), _i32,
+                                    C.c_uint32, _p, _sz, _p], C.c_int),
+        "aq_scales_to_canonical": ([W, _p, _p], C.c_int),
+        "aq_poll_device_status": ([_p], C.c_int),
+    }
+    for name, (args, res) in sigs.items():
+        fn = getattr(L, name)
+        fn.argtypes = args
+        fn.restype = res
+
+
+def last_error() -> str:
+    return lib().aq_last_error().decode()
+
+
+def check(status):
+    if status != OK:
+        raise AqError(status, last_error())
+    return status
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+# ------------------------------------------------------------ weights
+
+@dataclass
+class Nvfp4Weight:
+    """Device buffers of one NVFP4 weight [n, k] (allocated by torch)."""
+    n: int
+    k: int
+    packed: "object"        # uint8 [n*k/2]
+    scales: "object"        # uint8 [aq_scale_bytes(n, k)]
+    global_scale: "object"  # float32 [1]
+
+    @classmethod
+    def empty(cls, n, k, device="cuda"):
+        import torch
+        pb = lib().aq_packed_bytes(n, k)
+        sb = lib().aq_scale_bytes(n, k)
+        if pb == 0 or sb == 0:
+            raise AqError(ERR_SHAPE, "unsupported weight shape [%d, %d]" % (n, k))
+        return cls(n, k, torch.empty(pb, dtype=torch.uint8, device=device),
+                   torch.empty(sb, dtype=torch.uint8, device=device),
+                   torch.empty(1, dtype=torch.float32, device=device))
+
+    def c(self):
+        return Nvfp4WeightC(self.n, self.k, self.packed.data_ptr(),
+                            self.scales.data_ptr(), self.global_scale.data_ptr())
+
+    @property
+    def nbytes(self):
+        return self.packed.numel() + self.scales.numel()
+
+
+def packed_bytes(n, k):
+    return int(lib().aq_packed_bytes(n, k))
+
+
+def scale_bytes(n, k):
+    return int(lib().aq_scale_bytes(n, k))
+
+
+# ------------------------------------------------------------ calls
+
+def reconstruct(W0, s, U, V, W_eff, stream=None):
+    n, k = W0.shape
+    r = 0 if U is None else U.shape[1]
+    check(lib().aq_reconstruct(_ptr(W0), _ptr(s), _ptr(U), _ptr(V), n, k, r,
+                               _ptr(W_eff), _stream(stream)))
+
+
+def quantize_workspace_bytes():
+    return int(lib().aq_quantize_workspace_bytes())
+
+
+def quantize(W, out: Nvfp4Weight, workspace, stream=None):
+    n, k = W.shape
+    wc = out.c()
+    check(lib().aq_quantize_nvfp4(_ptr(W), n, k, C.byref(wc), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
+
+
+def reconstruct_quantize(W0, s, U, V, out: Nvfp4Weight, workspace, stream=None):
+    n, k = W0.shape
+    r = 0 if U is None else U.shape[1]
+    wc = out.c()
+    check(lib().aq_reconstruct_quantize_nvfp4(
+        _ptr(W0), _ptr(s), _ptr(U), _ptr(V), n, k, r, C.byref(wc), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def gemv_workspace_bytes(n, k, m=1):
+    b = int(lib().aq_gemv_workspace_bytes(n, k, m))
+    if b == 0:
+        raise AqError(ERR_SHAPE, last_error() or "bad GEMV shape")
+    return b
+
+
+def gemv(w: Nvfp4Weight, x, y, workspace, path=PATH_AUTO, stream=None):
+    m = x.shape[0]
+    wc = w.c()
+    check(lib().aq_gemv_nvfp4(C.byref(wc), _ptr(x), m, _ptr(y), path, _ptr(workspace),
+                              workspace.numel() * workspace.element_size(),
+                              _stream(stream)))
+
+
+class StepArgs:
+    """Host arrays of one decode step (kept alive while the step is reused)."""
+
+    def __init__(self, weights, xs, ys):
+        n = len(weights)
+        assert len(xs) == n and len(ys) == n
+        self.n = n
+        self.w = (Nvfp4WeightC * n)(*[w.c() for w in weights])
+        self.x = (C.c_void_p * n)(*[t.data_ptr() for t in xs])
+        self.y = (C.c_void_p * n)(*[t.data_ptr() for t in ys])
+        self.m = xs[0].shape[0] if n else 1
+
+
+def decode_step(args: StepArgs, workspace, flags=STEP_PDL, stream=None):
+    check(lib().aq_decode_step_weights(args.w, args.n, args.x, args.y, args.m, flags,
+                                       _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
+
+
+def scales_to_canonical(w: Nvfp4Weight, canon, stream=None):
+    wc = w.c()
+    check(lib().aq_scales_to_canonical(C.byref(wc), _ptr(canon), _stream(stream)))
+
+
+def poll_device_status(stream=None):
+    """Synchronises the stream; returns the aq_status code (does not raise)."""
+    return lib().aq_poll_device_status(_stream(stream))
