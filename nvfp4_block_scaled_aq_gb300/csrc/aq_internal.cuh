@@ -186,7 +186,8 @@ cudaError_t launch_scales_to_canonical(const aq_nvfp4_weight &w, uint8_t *canon,
 struct GemvPlan {
   int64_t row_blocks;  // ceil(n / rows_per_block)
   int64_t k_tiles;     // ceil(k / 128)
-  int64_t total;       // row_blocks * k_tiles work units
+  int64_t units;       // work units per row block
+  int64_t total;       // row_blocks * units
   int grid;            // persistent CTAs
   int max_contrib;     // most CTAs sharing one row block
 };

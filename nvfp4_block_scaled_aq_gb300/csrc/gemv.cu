@@ -40,27 +40,44 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <unordered_map>
 
 #include "aq_internal.cuh"
 
 namespace aq {
 namespace {
 
-constexpr int kW = 4;                  // consumer warps = row groups per CTA
-constexpr int kRB = 16 * kW;           // rows per row block
-constexpr int kStages = 8;             // TMA ring depth
+// Geometry of one work unit: a row block of kRB = 16 * kRG rows by kKT
+// k-tiles of 128 columns.  Consumer warp w owns row group (w % kRG) of the
+// block and k-tile (w / kRG) of the unit; the kKT warps of one row group
+// add their sums in a fixed order at the end of a segment.
+#ifndef AQ_GEMV_STAGES
+#define AQ_GEMV_STAGES 6
+#endif
+#ifndef AQ_GEMV_CTAS_PER_SM
+#define AQ_GEMV_CTAS_PER_SM 2
+#endif
+constexpr int kRG = 4;                          // row groups per row block
+constexpr int kKT = 2;                          // k-tiles per unit
+constexpr int kRB = 16 * kRG;                   // rows per row block
+constexpr int kW = kRG * kKT;                   // consumer warps
+constexpr int kStages = AQ_GEMV_STAGES;         // TMA ring depth
 constexpr int kThreads = (kW + 1) * 32;
-constexpr int kPackedStage = kRB * 64;             // bytes of nibbles per stage
-constexpr int kScaleStage = kW * 128;              // bytes of scales per stage
+constexpr int kUnitCols = 64 * kKT;             // packed bytes per row per unit
+constexpr int kPackedStage = kRB * kUnitCols;   // 8 KiB, 128-byte swizzled rows
+constexpr int kScaleStage = kRG * 128 * kKT;    // scale words of the unit
 constexpr int kStageBytes = kPackedStage + kScaleStage;
-constexpr int kXChunkBudget = 64;      // Mp * chunk_tiles
-constexpr int kTileHalves = 160;       // f16 per staged 128-column tile (padded)
+constexpr int kXChunkBudget = 16;               // m * units staged at once
+constexpr int kTileHalves = 160;                // f16 per staged 128-column tile (padded)
 constexpr unsigned kSpinLimit = 1u << 22;
+static_assert(kStageBytes % 1024 == 0, "128-byte swizzle needs 1 KiB-aligned stages");
+static_assert(kUnitCols == 128, "the swizzle pattern below assumes 128-byte rows");
 
 struct Smem {
-  alignas(128) uint8_t stage[kStages][kStageBytes];
+  alignas(1024) uint8_t stage[kStages][kStageBytes];
   alignas(8) uint64_t full[kStages];
   uint64_t empty[kStages];
+  float red[kRG][32][2][4];  // k-tile 1 sums handed to k-tile 0 warps
   uint32_t xmax[16];
   int shift[16];
   int flag;
@@ -143,11 +160,12 @@ struct GemvArgs {
   float *partial;      // [row_blocks][max_contrib][kRB][16]
   uint32_t *tickets;   // [row_blocks]
   unsigned *status;
-  int64_t total;       // row_blocks * k_tiles
+  int64_t total;       // row_blocks * units (work units of the launch)
   int n, k, m;
-  int k_tiles;
+  int k_tiles;         // ceil(k / 128)
+  int units;           // units per row block = ceil(k_tiles / kKT)
   int max_contrib;
-  int chunk_tiles;     // activation tiles staged at once
+  int chunk_units;     // units whose activations are staged at once
   int x_stride;        // f16 elements per staged token row
 };
 
@@ -155,13 +173,46 @@ struct GemvArgs {
 
 namespace {
 
+// One k-tile of one warp: decode the lane's two 16-byte nibble runs (rows g
+// and g+8, columns 32c..32c+31 of the tile), scale them by their block
+// scales in f16, and accumulate 8 m16n8k16 products per n8 block of tokens.
+// Even and odd k16 steps go to separate accumulators for latency overlap.
+template <int NT>
+__device__ __forceinline__ void tile_mma(float (&acc)[2][NT][4], const uint4 wlo,
+                                         const uint4 whi, uint32_t sw,
+                                         const uint32_t (&xr)[NT][16]) {
+  const uint32_t s01 = e4m3x2_to_f16x2(uint16_t(sw & 0xFFFFu));
+  const uint32_t s23 = e4m3x2_to_f16x2(uint16_t(sw >> 16));
+  const uint32_t sa0 = __byte_perm(s01, 0, 0x1010), sa1 = __byte_perm(s01, 0, 0x3232);
+  const uint32_t sb0 = __byte_perm(s23, 0, 0x1010), sb1 = __byte_perm(s23, 0, 0x3232);
+  const uint32_t lo[4] = {wlo.x, wlo.y, wlo.z, wlo.w};
+  const uint32_t hi[4] = {whi.x, whi.y, whi.z, whi.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t fl[4], fh[4];
+    e2m1x8_to_f16x2x4(lo[q], fl);
+    e2m1x8_to_f16x2x4(hi[q], fh);
+    const uint32_t sa = q < 2 ? sa0 : sa1, sb = q < 2 ? sb0 : sb1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t A[4] = {hmul2(fl[2 * h], sa), hmul2(fh[2 * h], sb),
+                             hmul2(fl[2 * h + 1], sa), hmul2(fh[2 * h + 1], sb)};
+      const int s = 2 * q + h;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) mma_16816(acc[h][nt], A, xr[nt][2 * s], xr[nt][2 * s + 1]);
+    }
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kThreads)
     gemv_kernel(const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_s, const GemvArgs a) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  Smem &sm = *reinterpret_cast<Smem *>(smem_raw);
-  uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw + sizeof(Smem));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // The 128-byte swizzle of the weight stages needs a 1 KiB-aligned base.
+  uint8_t *smem_base = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  Smem &sm = *reinterpret_cast<Smem *>(smem_base);
+  uint16_t *xs = reinterpret_cast<uint16_t *>(smem_base + sizeof(Smem));
   volatile int *aborted = &sm.aborted;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -183,6 +234,8 @@ __global__ void __launch_bounds__(kThreads)
   // ------------------------------------------------------------ producer
   if (warp == kW) {
     if (lane == 0) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s)) : "memory");
       int64_t issued = 0;
       for (int64_t j = 0; u_begin + j < u_end; ++j) {
         const int st = int(j % kStages);
@@ -196,11 +249,12 @@ __global__ void __launch_bounds__(kThreads)
         }
         if (*aborted) break;
         const int64_t u = u_begin + j;
-        const int64_t rb = u / a.k_tiles;
-        const int t = int(u - rb * a.k_tiles);
+        const int64_t rb = u / a.units;
+        const int uk = int(u - rb * a.units);
         mbar_expect_tx(&sm.full[st], kStageBytes);
-        tma_load_2d(sm.stage[st], &tm_w, t * 64, int(rb * kRB), &sm.full[st]);
-        tma_load_2d(sm.stage[st] + kPackedStage, &tm_s, t * 128, int(rb * kW), &sm.full[st]);
+        tma_load_2d(sm.stage[st], &tm_w, uk * kUnitCols, int(rb * kRB), &sm.full[st]);
+        tma_load_2d(sm.stage[st] + kPackedStage, &tm_s, uk * kScaleStage / kRG, int(rb * kRG),
+                    &sm.full[st]);
         issued = j + 1;
       }
       // No copy may still be landing in shared memory when the CTA exits:
@@ -214,20 +268,25 @@ __global__ void __launch_bounds__(kThreads)
 
   // ------------------------------------------------------------ consumers
   const int g = lane >> 2, c = lane & 3;
-  pdl_wait();  // x (and the workspace) may come from the previous kernel
+  const int rg = warp % kRG, kt = warp / kRG;
+  // 128-byte swizzle: logical 16-byte chunk ch of row r sits at ch ^ (r & 7).
+  const int off_lo = (rg * 16 + g) * kUnitCols + (((kt * 4 + c) ^ (g & 7)) << 4);
+  const int off_hi = (rg * 16 + g + 8) * kUnitCols + (((kt * 4 + c) ^ ((g + 8) & 7)) << 4);
+  const int off_sc = kPackedStage + (rg * kKT + kt) * 128 + lane * 4;
+  pdl_wait();  // x and the workspace may come from the previous kernel
   const float gd = __ldg(a.g_dec);
   int64_t j = 0;
   int64_t u = u_begin;
   while (u < u_end) {
-    const int64_t rb = u / a.k_tiles;
-    const int t0 = int(u - rb * a.k_tiles);
-    const int t1 = int(t0 + (u_end - u) < a.k_tiles ? t0 + (u_end - u) : a.k_tiles);
+    const int64_t rb = u / a.units;
+    const int uk0 = int(u - rb * a.units);
+    const int uk1 = int(uk0 + (u_end - u) < a.units ? uk0 + (u_end - u) : a.units);
 
     // -- per-token exponent of this segment's activations
     if (threadIdx.x < 16) sm.xmax[threadIdx.x] = 0;
     consumer_sync();
     {
-      const int k0 = t0 * 128, k1 = min(t1 * 128, a.k);
+      const int k0 = uk0 * kUnitCols * 2, k1 = min(uk1 * kUnitCols * 2, a.k);
       const int nvec = (k1 - k0) / 8;
       for (int tok = 0; tok < a.m; ++tok) {
         const uint4 *xv = reinterpret_cast<const uint4 *>(a.x + int64_t(tok) * a.k + k0);
@@ -253,21 +312,24 @@ __global__ void __launch_bounds__(kThreads)
       sm.shift[threadIdx.x] = sh;
     }
 
-    float acc[NT][4];
+    float acc[2][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[h][nt][i] = 0.0f;
 
-    for (int cc0 = t0; cc0 < t1; cc0 += a.chunk_tiles) {
-      const int cc1 = min(t1, cc0 + a.chunk_tiles);
+    for (int cu0 = uk0; cu0 < uk1; cu0 += a.chunk_units) {
+      const int cu1 = min(uk1, cu0 + a.chunk_units);
       consumer_sync();  // earlier readers of the staging buffer are done
-      // -- stage x[:, cc0*128 .. cc1*128) as scaled f16
+      // -- stage x[:, k-tiles of units cu0..cu1) as scaled f16 (zero past k)
       {
-        const int nv = (cc1 - cc0) * 16;  // 8-element vectors per token
+        const int nv = (cu1 - cu0) * kKT * 16;  // 8-element vectors per token
+        const int kbase = cu0 * kKT * 128;
         for (int idx = threadIdx.x; idx < a.m * nv; idx += kW * 32) {
           const int tok = idx / nv, v = idx - tok * nv;
-          const int e = v * 8, kk = cc0 * 128 + e;
+          const int e = v * 8, kk = kbase + e;
           uint4 q = make_uint4(0, 0, 0, 0);
           if (kk < a.k)
             q = __ldg(reinterpret_cast<const uint4 *>(a.x + int64_t(tok) * a.k + kk));
@@ -284,7 +346,7 @@ __global__ void __launch_bounds__(kThreads)
       }
       consumer_sync();
 
-      for (int t = cc0; t < cc1; ++t, ++j) {
+      for (int uk = cu0; uk < cu1; ++uk, ++j) {
         const int st = int(j % kStages);
         uint4 wlo = make_uint4(0, 0, 0, 0), whi = make_uint4(0, 0, 0, 0);
         uint32_t sw = 0;
@@ -292,9 +354,9 @@ __global__ void __launch_bounds__(kThreads)
                         mbar_wait(&sm.full[st], unsigned(j / kStages) & 1u, aborted);
         if (ok) {
           const uint8_t *base = sm.stage[st];
-          wlo = *reinterpret_cast<const uint4 *>(base + (warp * 16 + g) * 64 + 16 * c);
-          whi = *reinterpret_cast<const uint4 *>(base + (warp * 16 + g + 8) * 64 + 16 * c);
-          sw = *reinterpret_cast<const uint32_t *>(base + kPackedStage + warp * 128 + lane * 4);
+          wlo = *reinterpret_cast<const uint4 *>(base + off_lo);
+          whi = *reinterpret_cast<const uint4 *>(base + off_hi);
+          sw = *reinterpret_cast<const uint32_t *>(base + off_sc);
         } else if (lane == 0 && !*aborted) {
           *aborted = 1;
           raise_status(a.status, kDevTimeout);
@@ -302,8 +364,8 @@ __global__ void __launch_bounds__(kThreads)
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.empty[st]);
 
-        // -- activations of this tile for the tokens of each n8 block
-        const int tl = t - cc0;
+        // -- activations of this warp's k-tile for each n8 block of tokens
+        const int tl = (uk - cu0) * kKT + kt;
         uint32_t xr[NT][16];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -319,52 +381,53 @@ __global__ void __launch_bounds__(kThreads)
             xr[nt][4 * q + 3] = v.w;
           }
         }
-        // -- block scales as f16 pairs: rows g / g+8, blocks 2c / 2c+1
-        const uint32_t s01 = e4m3x2_to_f16x2(uint16_t(sw & 0xFFFFu));
-        const uint32_t s23 = e4m3x2_to_f16x2(uint16_t(sw >> 16));
-        const uint32_t sa0 = __byte_perm(s01, 0, 0x1010), sa1 = __byte_perm(s01, 0, 0x3232);
-        const uint32_t sb0 = __byte_perm(s23, 0, 0x1010), sb1 = __byte_perm(s23, 0, 0x3232);
-        const uint32_t lo[4] = {wlo.x, wlo.y, wlo.z, wlo.w};
-        const uint32_t hi[4] = {whi.x, whi.y, whi.z, whi.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t fl[4], fh[4];
-          e2m1x8_to_f16x2x4(lo[q], fl);
-          e2m1x8_to_f16x2x4(hi[q], fh);
-          const uint32_t sa = q < 2 ? sa0 : sa1, sb = q < 2 ? sb0 : sb1;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t A[4] = {hmul2(fl[2 * h], sa), hmul2(fh[2 * h], sb),
-                                   hmul2(fl[2 * h + 1], sa), hmul2(fh[2 * h + 1], sb)};
-            const int s = 2 * q + h;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) mma_16816(acc[nt], A, xr[nt][2 * s], xr[nt][2 * s + 1]);
-          }
-        }
+        tile_mma<NT>(acc, wlo, whi, sw, xr);
       }
     }
 
-    // -- epilogue: this warp holds rows g, g+8 x tokens nt*8 + 2c + {0,1}
-    const bool complete = (t0 == 0 && t1 == a.k_tiles);
-    const int64_t unit0 = rb * a.k_tiles;
-    const int64_t own_lo = owner_of(unit0, a.total, grid);
-    const int contrib = int(owner_of(unit0 + a.k_tiles - 1, a.total, grid) - own_lo + 1);
-    const int jj = int(blockIdx.x - own_lo);
+    // -- fold: even/odd accumulators, then k-tile 1 warps into k-tile 0 warps
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int token = nt * 8 + 2 * c + (i & 1);
-        const int row_local = warp * 16 + g + 8 * (i >> 1);
-        if (token >= a.m) continue;
-        const float p = mul_pow2(acc[nt][i], -sm.shift[token]);
-        if (complete) {
-          const int64_t row = rb * kRB + row_local;
-          if (row < a.n) a.y[int64_t(token) * a.n + row] = f32_to_bf16_rn(__fmul_rn(p, gd));
-        } else {
-          a.partial[((rb * a.max_contrib + jj) * kRB + row_local) * 16 + token] = p;
+      for (int i = 0; i < 4; ++i) acc[0][nt][i] = __fadd_rn(acc[0][nt][i], acc[1][nt][i]);
+    if (kt == 1) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sm.red[rg][lane][nt][i] = acc[0][nt][i];
+    }
+    consumer_sync();
+    if (kt == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          acc[0][nt][i] = __fadd_rn(acc[0][nt][i], sm.red[rg][lane][nt][i]);
+    }
+
+    // -- epilogue: k-tile-0 warps hold rows g, g+8 x tokens nt*8 + 2c + {0,1}
+    const bool complete = (uk0 == 0 && uk1 == a.units);
+    const int64_t unit0 = rb * a.units;
+    const int64_t own_lo = owner_of(unit0, a.total, grid);
+    const int contrib = int(owner_of(unit0 + a.units - 1, a.total, grid) - own_lo + 1);
+    const int jj = int(blockIdx.x - own_lo);
+    if (kt == 0) {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int token = nt * 8 + 2 * c + (i & 1);
+          const int row_local = rg * 16 + g + 8 * (i >> 1);
+          if (token >= a.m) continue;
+          const float p = mul_pow2(acc[0][nt][i], -sm.shift[token]);
+          if (complete) {
+            const int64_t row = rb * kRB + row_local;
+            if (row < a.n) a.y[int64_t(token) * a.n + row] = f32_to_bf16_rn(__fmul_rn(p, gd));
+          } else {
+            a.partial[((rb * a.max_contrib + jj) * kRB + row_local) * 16 + token] = p;
+          }
         }
-      }
+    }
     if (!complete) {
       __threadfence();
       consumer_sync();
@@ -388,7 +451,7 @@ __global__ void __launch_bounds__(kThreads)
         if (threadIdx.x == 0) a.tickets[rb] = 0;
       }
     }
-    u += t1 - t0;
+    u += uk1 - uk0;
   }
 }
 
@@ -416,23 +479,62 @@ bool encoder() {
 // 2-D uint8 tensor [rows, cols] with a row pitch of `pitch` bytes, copied
 // in boxes of box_cols x box_rows; out-of-range box parts read as zero.
 bool make_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
-              uint64_t pitch, uint32_t box_cols, uint32_t box_rows) {
+              uint64_t pitch, uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
   const cuuint64_t dims[2] = {cols, rows};
   const cuuint64_t strides[1] = {pitch};
   const cuuint32_t box[2] = {box_cols, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int chunk_tiles_for(int m) { return m >= 32 ? 2 : (kXChunkBudget / m < 2 ? 2 : kXChunkBudget / m); }
+// Encoded tensor maps are a pure function of (base, shape, box), so an
+// exact-key cache can never return a stale map; it saves the encode on
+// every launch of a decode step.
+struct MapKey {
+  uintptr_t base;
+  uint64_t cols, rows;
+  uint32_t box_rows;
+  bool operator==(const MapKey &o) const {
+    return base == o.base && cols == o.cols && rows == o.rows && box_rows == o.box_rows;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey &k) const {
+    return std::hash<uintptr_t>()(k.base) ^ (std::hash<uint64_t>()(k.cols * 1000003u + k.rows) << 1) ^
+           k.box_rows;
+  }
+};
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
 
-size_t smem_bytes_for(int m) {
-  const int x_stride = chunk_tiles_for(m) * kTileHalves + 8;
-  return sizeof(Smem) + size_t(m) * x_stride * 2;
+bool cached_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                uint32_t box_cols, uint32_t box_rows, bool swizzle128) {
+  const MapKey key{reinterpret_cast<uintptr_t>(base), cols, rows,
+                   box_rows * 2u + (swizzle128 ? 1u : 0u)};
+  {
+    std::lock_guard<std::mutex> lock(g_map_mu);
+    auto it = g_maps.find(key);
+    if (it != g_maps.end()) {
+      *map = it->second;
+      return true;
+    }
+  }
+  if (!make_map(map, base, cols, rows, cols, box_cols, box_rows, swizzle128)) return false;
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  if (g_maps.size() > 65536) g_maps.clear();
+  g_maps.emplace(key, *map);
+  return true;
 }
+
+int chunk_units_for(int m) { return kXChunkBudget / m < 1 ? 1 : kXChunkBudget / m; }
+
+int x_stride_for(int m) { return chunk_units_for(m) * kKT * kTileHalves + 8; }
+
+size_t smem_bytes_for(int m) { return 1024 + sizeof(Smem) + size_t(m) * x_stride_for(m) * 2; }
 
 template <int NT>
 cudaError_t set_smem_attr(int device) {
@@ -455,18 +557,18 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev) {
   GemvPlan p;
   p.row_blocks = ceil_div(n, kRB);
   p.k_tiles = ceil_div(k, kTileCols);
-  p.total = p.row_blocks * p.k_tiles;
-  // Two resident CTAs per SM leave room for the next projection's CTAs
-  // to start early under programmatic dependent launch; at least two
-  // tiles per CTA so tiny projections do not drown in epilogues.
-  int64_t g = int64_t(dev.sms) * 2;
-  const int64_t cap = ceil_div(p.total, 2);
-  if (g > cap) g = cap;
+  p.units = ceil_div(p.k_tiles, kKT);
+  p.total = p.row_blocks * p.units;
+  // Two resident CTAs per SM keep ~100 KiB of weights in flight per SM and
+  // leave room for one CTA of the next projection to start early under
+  // programmatic dependent launch.  Tiny projections get one unit per CTA.
+  int64_t g = int64_t(dev.sms) * AQ_GEMV_CTAS_PER_SM;
+  if (g > p.total) g = p.total;
   if (g < 1) g = 1;
   p.grid = int(g);
   int worst = 1;
   for (int64_t rb = 0; rb < p.row_blocks; ++rb) {
-    const int64_t u0 = rb * p.k_tiles, u1 = u0 + p.k_tiles - 1;
+    const int64_t u0 = rb * p.units, u1 = u0 + p.units - 1;
     const int c = int(owner_of(u1, p.total, g) - owner_of(u0, p.total, g) + 1);
     if (c > worst) worst = c;
   }
@@ -474,10 +576,15 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev) {
   return p;
 }
 
+// Workspace layout: a ticket region of fixed size at the start (one 32-bit
+// ticket per row block of the largest legal n), then the fp32 partials.
+// The fixed offset keeps the tickets of every shape clear of the partials
+// of every other shape, so one zeroed workspace serves calls of any shape.
+constexpr size_t kTicketBytes = size_t(((1 << 24) + kRB - 1) / kRB) * 4;
+
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev) {
   const GemvPlan p = plan_gemv(n, k, dev);
-  const size_t tickets = size_t(ceil_div(p.row_blocks * 4, 256) * 256);
-  return tickets + size_t(p.row_blocks) * p.max_contrib * kRB * 16 * sizeof(float);
+  return kTicketBytes + size_t(p.row_blocks) * p.max_contrib * kRB * 16 * sizeof(float);
 }
 
 cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
@@ -485,10 +592,11 @@ cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint
   if (!encoder()) return cudaErrorNotSupported;
   const GemvPlan p = plan_gemv(w.n, w.k, dev);
   CUtensorMap tm_w, tm_s;
-  if (!make_map(&tm_w, w.packed, uint64_t(w.k) / 2, uint64_t(w.n), uint64_t(w.k) / 2, 64, kRB))
+  if (!cached_map(&tm_w, w.packed, uint64_t(w.k) / 2, uint64_t(w.n), kUnitCols, kRB, true))
     return cudaErrorInvalidValue;
   const uint64_t srow = uint64_t(p.k_tiles) * 128;
-  if (!make_map(&tm_s, w.scales, srow, uint64_t(ceil_div(w.n, kTileRows)), srow, 128, kW))
+  if (!cached_map(&tm_s, w.scales, srow, uint64_t(ceil_div(w.n, kTileRows)), kScaleStage / kRG,
+                  kRG, false))
     return cudaErrorInvalidValue;
 
   GemvArgs a;
@@ -497,16 +605,17 @@ cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint
   a.y = y;
   uint8_t *base = static_cast<uint8_t *>(ws);
   a.tickets = reinterpret_cast<uint32_t *>(base);
-  a.partial = reinterpret_cast<float *>(base + ceil_div(p.row_blocks * 4, 256) * 256);
+  a.partial = reinterpret_cast<float *>(base + kTicketBytes);
   a.status = dev.status;
   a.total = p.total;
   a.n = w.n;
   a.k = w.k;
   a.m = m;
   a.k_tiles = int(p.k_tiles);
+  a.units = int(p.units);
   a.max_contrib = p.max_contrib;
-  a.chunk_tiles = chunk_tiles_for(m);
-  a.x_stride = a.chunk_tiles * kTileHalves + 8;
+  a.chunk_units = chunk_units_for(m);
+  a.x_stride = x_stride_for(m);
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);

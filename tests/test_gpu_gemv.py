@@ -77,9 +77,24 @@ def test_gemv_is_deterministic_and_workspace_rearms():
     ys = [gemv_gpu(w, x, ws) for _ in range(4)]
     for y in ys[1:]:
         assert torch.equal(y, ys[0])
-    # the split-K tickets are back at zero after every call
-    plan_tickets = ws[:256].view(torch.int32)
-    assert int(plan_tickets.abs().sum()) == 0
+    # the split-K tickets (fixed 1 MiB region at the start) are back at zero
+    assert int(ws[: 1 << 20].view(torch.int32).abs().sum()) == 0
+
+
+def test_one_workspace_serves_interleaved_shapes():
+    """Calls of different shapes share one zeroed workspace in any order."""
+    shapes = [(1536, 1152), (1152, 6912), (13824, 1152), (1152, 1024)]
+    ws_bytes = max(aq.gemv_workspace_bytes(n, k, 1) for n, k in shapes)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=DEV)
+    cases = []
+    for i, (n, k) in enumerate(shapes):
+        w = quantize_gpu(inputs.weight(n, k, seed=40 + i, device=DEV))
+        x = inputs.tokens(1, k, seed=50 + i, device=DEV)
+        cases.append((w, x, gemv_gpu(w, x)))
+    for order in ([0, 1, 2, 3], [3, 1, 0, 2, 1, 3, 2, 0]):
+        for i in order:
+            w, x, want = cases[i]
+            assert torch.equal(gemv_gpu(w, x, ws), want), i
 
 
 def test_gemv_power_of_two_input_scaling_is_exact():
