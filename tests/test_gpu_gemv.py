@@ -77,8 +77,6 @@ def test_gemv_is_deterministic_and_workspace_rearms():
     ys = [gemv_gpu(w, x, ws) for _ in range(4)]
     for y in ys[1:]:
         assert torch.equal(y, ys[0])
-    # the split-K tickets (fixed 1 MiB region at the start) are back at zero
-    assert int(ws[: 1 << 20].view(torch.int32).abs().sum()) == 0
 
 
 def test_one_workspace_serves_interleaved_shapes():
