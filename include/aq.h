@@ -187,6 +187,36 @@ AQ_API aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj
                                  int32_t m, uint32_t flags, void *workspace,
                                  size_t workspace_bytes, aq_stream_t stream);
 
+/* The decode step's weight stream as ONE persistent kernel ("GPU
+ * acceleration", "CUDA graph capture": replay the step without per-kernel
+ * dispatch; "Q/K/V fusion": one weight read per fused projection).
+ *
+ * aq_step_plan_create validates the projections exactly like
+ * aq_decode_step_weights, encodes their tensor maps and stream-K
+ * partitions, and uploads them (synchronously, cudaMemcpy) into `plan`:
+ * device memory of aq_step_plan_bytes(n_proj) bytes, 128-byte aligned,
+ * owned by the caller and read by every aq_step_run until the caller frees
+ * it.  The weight, x and y pointers are baked into the plan, so the buffers
+ * must stay allocated and keep their addresses.  *workspace_bytes receives
+ * the workspace size aq_step_run needs; that workspace must be zero-filled
+ * once after allocation and is left ready for the next run.
+ *
+ * aq_step_run computes, for p = 0 .. n_proj-1 in order,
+ * y[p] = GEMV(w[p], x[p]) with the m tokens the plan was made for, in one
+ * cooperative launch on `stream`: every CTA streams the weights of all
+ * projections back to back, and before reading x[p] it waits (grid-wide,
+ * bounded) until every output of projection p-1 is written.  Results equal
+ * the per-projection calls to within the GEMV tolerance (the split over K
+ * can differ).  A plan, m or workspace that does not match is reported by
+ * the next aq_poll_device_status() as AQ_ERR_INVALID_ARG.  Safe to record
+ * into a CUDA graph; runs that may overlap need separate workspaces. */
+AQ_API size_t aq_step_plan_bytes(int32_t n_proj);
+AQ_API aq_status aq_step_plan_create(const aq_nvfp4_weight *w, int32_t n_proj,
+                                     const uint16_t *const *x, uint16_t *const *y, int32_t m,
+                                     void *plan, size_t plan_bytes, size_t *workspace_bytes);
+AQ_API aq_status aq_step_run(const void *plan, int32_t m, void *workspace,
+                             size_t workspace_bytes, aq_stream_t stream);
+
 /* Test helper: the scales of w rewritten in canonical row-major order
  * [n, k/16] into canon (device, n*k/16 bytes). */
 AQ_API aq_status aq_scales_to_canonical(const aq_nvfp4_weight *w, uint8_t *canon,

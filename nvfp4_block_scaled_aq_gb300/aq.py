@@ -84,6 +84,10 @@ def _declare(L):
         "aq_decode_step_weights": ([W, _i32, C.POINTER(_p), C.POINTER(_p), _i32,
                                     C.c_uint32, _p, _sz, _p], C.c_int),
         "aq_scales_to_canonical": ([W, _p, _p], C.c_int),
+        "aq_step_plan_bytes": ([_i32], _sz),
+        "aq_step_plan_create": ([W, _i32, C.POINTER(_p), C.POINTER(_p), _i32, _p, _sz,
+                                 C.POINTER(_sz)], C.c_int),
+        "aq_step_run": ([_p, _i32, _p, _sz, _p], C.c_int),
         "aq_poll_device_status": ([_p], C.c_int),
     }
     for name, (args, res) in sigs.items():
@@ -215,6 +219,35 @@ def decode_step(args: StepArgs, workspace, flags=STEP_PDL, stream=None):
                                        _ptr(workspace),
                                        workspace.numel() * workspace.element_size(),
                                        _stream(stream)))
+
+
+class StepPlan:
+    """A persistent decode-step plan: device buffer written once by
+    aq_step_plan_create.  Keeps the weights and activation buffers it
+    points to alive."""
+
+    def __init__(self, weights, xs, ys):
+        import torch
+        self.args = StepArgs(weights, xs, ys)
+        self.keep = (list(weights), list(xs), list(ys))
+        self.m = self.args.m
+        nbytes = int(lib().aq_step_plan_bytes(self.args.n))
+        if nbytes == 0:
+            raise AqError(ERR_INVALID_ARG, "bad projection count")
+        self.buf = torch.empty(nbytes, dtype=torch.uint8, device=xs[0].device)
+        ws = C.c_size_t(0)
+        check(lib().aq_step_plan_create(self.args.w, self.args.n, self.args.x, self.args.y,
+                                        self.m, _ptr(self.buf), nbytes, C.byref(ws)))
+        self.workspace_bytes = int(ws.value)
+
+    def workspace(self):
+        import torch
+        return torch.zeros(self.workspace_bytes, dtype=torch.uint8, device=self.buf.device)
+
+
+def step_run(plan: StepPlan, workspace, m=None, stream=None):
+    check(lib().aq_step_run(_ptr(plan.buf), plan.m if m is None else m, _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def scales_to_canonical(w: Nvfp4Weight, canon, stream=None):

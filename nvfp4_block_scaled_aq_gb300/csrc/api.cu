@@ -287,6 +287,51 @@ aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,
   return AQ_OK;
 }
 
+size_t aq_step_plan_bytes(int32_t n_proj) {
+  if (n_proj < 1 || n_proj > (1 << 20)) return 0;
+  return step_plan_bytes(n_proj);
+}
+
+aq_status aq_step_plan_create(const aq_nvfp4_weight *w, int32_t n_proj, const uint16_t *const *x,
+                              uint16_t *const *y, int32_t m, void *plan, size_t plan_bytes,
+                              size_t *workspace_bytes) {
+  const char *what = "aq_step_plan_create";
+  if (n_proj < 1 || n_proj > (1 << 20))
+    return set_error(AQ_ERR_INVALID_ARG, "%s: n_proj = %d outside [1, 2^20]", what, n_proj);
+  if (!w || !x || !y || !plan)
+    return set_error(AQ_ERR_INVALID_ARG, "%s: w, x, y and plan must not be NULL", what);
+  if (!aligned(plan, 128)) return set_error(AQ_ERR_ALIGNMENT, "%s: plan must be 128-byte aligned", what);
+  for (int32_t p = 0; p < n_proj; ++p) {
+    aq_status s = gemv_args(&w[p], x[p], m, y[p], AQ_PATH_GEMV, what);
+    if (s != AQ_OK) {
+      char msg[sizeof t_err];
+      std::strncpy(msg, t_err, sizeof msg - 1);
+      msg[sizeof msg - 1] = 0;
+      return set_error(s, "projection %d: %s", p, msg);
+    }
+  }
+  const DeviceInfo *dev = device_info();
+  if (!dev) return AQ_ERR_UNSUPPORTED;
+  return step_plan_create(w, n_proj, x, y, m, plan, plan_bytes, workspace_bytes, *dev);
+}
+
+aq_status aq_step_run(const void *plan, int32_t m, void *workspace, size_t workspace_bytes,
+                      aq_stream_t stream) {
+  const char *what = "aq_step_run";
+  if (!plan || !workspace)
+    return set_error(AQ_ERR_INVALID_ARG, "%s: plan and workspace must not be NULL", what);
+  if (!aligned(plan, 128)) return set_error(AQ_ERR_ALIGNMENT, "%s: plan must be 128-byte aligned", what);
+  if (!aligned(workspace, 256))
+    return set_error(AQ_ERR_WORKSPACE, "%s: workspace must be 256-byte aligned", what);
+  if (m < 1 || m > AQ_MAX_M)
+    return set_error(AQ_ERR_SHAPE, "%s: m = %d outside [1, %d]", what, m, AQ_MAX_M);
+  const DeviceInfo *dev = device_info();
+  if (!dev) return AQ_ERR_UNSUPPORTED;
+  return launched(launch_step(plan, m, workspace, workspace_bytes, *dev,
+                              reinterpret_cast<cudaStream_t>(stream)),
+                  what);
+}
+
 aq_status aq_scales_to_canonical(const aq_nvfp4_weight *w, uint8_t *canon, aq_stream_t stream) {
   aq_status s = check_weight(w, "aq_scales_to_canonical");
   if (s != AQ_OK) return s;
@@ -317,6 +362,9 @@ aq_status aq_poll_device_status(aq_stream_t stream) {
       return set_error(AQ_ERR_RANGE, "per-tensor amax was non-finite or too small to scale");
     case kDevTimeout:
       return set_error(AQ_ERR_TIMEOUT, "a bounded device-side wait gave up; re-zero GEMV workspaces");
+    case kDevBadPlan:
+      return set_error(AQ_ERR_INVALID_ARG,
+                       "aq_step_run: plan, m, grid or workspace size do not match the plan");
     default:
       return set_error(AQ_ERR_CUDA, "unknown device status %u", word);
   }

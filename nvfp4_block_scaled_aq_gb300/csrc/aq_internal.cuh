@@ -12,7 +12,7 @@ namespace aq {
 // ------------------------------------------------------------ status word
 // One 32-bit word per device records the first device-detected condition
 // since the last poll (0 = none).  Kernels receive its address.
-enum : unsigned { kDevOk = 0, kDevRange = 1, kDevTimeout = 2 };
+enum : unsigned { kDevOk = 0, kDevRange = 1, kDevTimeout = 2, kDevBadPlan = 3 };
 
 __device__ __forceinline__ void raise_status(unsigned *status, unsigned code) {
   atomicCAS(status, 0u, code);
@@ -195,5 +195,12 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev);
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev);
 cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
                         void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st);
+
+size_t step_plan_bytes(int n_proj);
+aq_status step_plan_create(const aq_nvfp4_weight *w, int n_proj, const uint16_t *const *x,
+                           uint16_t *const *y, int m, void *plan, size_t plan_bytes,
+                           size_t *ws_bytes, const DeviceInfo &dev);
+cudaError_t launch_step(const void *plan, int m, void *ws, size_t ws_bytes, const DeviceInfo &dev,
+                        cudaStream_t st);
 
 }  // namespace aq

@@ -1,0 +1,547 @@
+// gemv_core.cuh -- device code shared by the single-projection GEMV kernel
+// (gemv.cu) and the persistent decode-step kernel (step.cu): the TMA ring,
+// the producer loop, and the consumer loop that dequantises NVFP4 weights
+// in registers and accumulates with mma.sync.
+//
+// Method: Weightless docs, "GPU and cache acceleration", "Future work" (a
+// GEMV that dequantises 4-bit weights in registers and streams at full HBM
+// bandwidth); AttnQuant docs, "Throughput", per-kernel MLP analysis
+// (split-K for skinny projections).  Design notes are in gemv.cu.
+#pragma once
+
+#include <cuda.h>
+
+#include "aq_internal.cuh"
+
+namespace aq {
+namespace core {
+
+constexpr int kRG = 8;                          // row groups (consumer warps) per CTA
+constexpr int kKT = 2;                          // k-tiles per unit
+constexpr int kRB = 16 * kRG;                   // rows per row block (128)
+constexpr int kW = kRG;                         // consumer warps
+constexpr int kThreads = (kW + 1) * 32;
+constexpr int kUnitCols = 64 * kKT;             // packed bytes per row per unit (128)
+constexpr int kUnitK = 128 * kKT;               // k columns per unit (256)
+constexpr int kPackedStage = kRB * kUnitCols;   // 16 KiB, 128-byte swizzled rows
+constexpr int kScaleStage = kRG * 128 * kKT;    // 2 KiB of scale words
+constexpr int kStageBytes = kPackedStage + kScaleStage;
+constexpr int kMaxStages = 6;
+constexpr int kMinStages = 2;
+constexpr int kCtasPerSm = 2;
+constexpr int kSmemBudget = 113 * 1024;         // per CTA, so two fit on an SM
+constexpr int kXChunkBudget = 16;               // m * units staged at once (chunked mode)
+constexpr int kTileHalves = 128;                // f16 per staged 128-column tile
+constexpr unsigned kSpinLimit = 1u << 22;
+// Ticket region of fixed size at the start of a GEMV workspace (one 32-bit
+// ticket per row block of the largest legal n), then the fp32 partials.
+constexpr size_t kTicketBytes = size_t(((1 << 24) + kRB - 1) / kRB) * 4;
+static_assert(kStageBytes % 1024 == 0, "128-byte swizzle needs 1 KiB-aligned stages");
+static_assert(kUnitCols == 128, "the swizzle pattern assumes 128-byte rows");
+
+// Control block that follows the ring in shared memory.
+struct Ctrl {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  uint32_t xmax[16];
+  int shift[16];
+  int flag;
+  int aborted;
+};
+constexpr int kCtrlBytes = (int(sizeof(Ctrl)) + 15) / 16 * 16;
+
+// Position in the ring, advanced once per unit (no division on the hot
+// path): stage index, parity of the current pass over the ring, and
+// whether the ring has been through one full pass.
+struct RingPos {
+  int st = 0;
+  unsigned phase = 0;
+  bool wrapped = false;
+  int64_t count = 0;  // units passed so far
+  __host__ __device__ __forceinline__ void advance(int S) {
+    ++count;
+    if (++st == S) {
+      st = 0;
+      phase ^= 1u;
+      wrapped = true;
+    }
+  }
+};
+
+// One projection as the kernels see it.
+struct Proj {
+  const CUtensorMap *tm_w;  // packed nibbles [n, k/2], box 128 B x 128 rows, 128B swizzle
+  const CUtensorMap *tm_s;  // scale words [ceil(n/16), ceil(k/128)*128], box 256 B x 8 rows
+  const float *g_dec;
+  const uint16_t *x;        // [m, k] bf16
+  uint16_t *y;              // [m, n] bf16
+  int64_t total;            // row_blocks * units
+  int n, k;
+  int units;                // units per row block
+  int max_contrib;          // most CTAs sharing a row block
+  int grid;                 // CTAs that share this projection (<= total); the
+                            // rest of the launch sits it out
+};
+
+// Per-launch state.
+struct Run {
+  float *partial;           // [row_blocks][max_contrib][kRB][16]
+  uint32_t *tickets;        // [row_blocks]
+  unsigned *status;
+  int m;
+  int stages;
+  int x_cap;                // f16 capacity of the activation staging buffer
+};
+
+__host__ __device__ __forceinline__ int64_t range_begin(int64_t i, int64_t total, int64_t grid) {
+  return (i * total) / grid;
+}
+__host__ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t total, int64_t grid) {
+  return ((u + 1) * grid - 1) / total;
+}
+
+// Activations a CTA stages for its unit range [u_begin, u_end): the
+// `slots` distinct units of k it touches (all units if the range is at
+// least a row block long), each 256 columns, per token.
+__host__ __device__ __forceinline__ int x_slots(int64_t range, int units) {
+  return range >= units ? units : int(range);
+}
+__host__ __device__ __forceinline__ int x_stride_full(int slots) {
+  return slots * 2 * kTileHalves + 8;  // +8 f16 spreads tokens over banks
+}
+__host__ __device__ __forceinline__ int chunk_units_for(int m) {
+  return kXChunkBudget / m < 1 ? 1 : kXChunkBudget / m;
+}
+__host__ __device__ __forceinline__ int x_stride_chunk(int m) {
+  return chunk_units_for(m) * 2 * kTileHalves + 8;
+}
+
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Bounded wait for the phase with the given parity; false on give-up.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
+                                          volatile int *aborted) {
+  const uint32_t addr = smem_u32(bar);
+  for (unsigned it = 0; it < kSpinLimit; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p;\n"
+        "  mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "  selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 1023u) == 1023u && *aborted) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Consumer-warps-only barrier (the producer warp never joins it).
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kW * 32) : "memory");
+}
+
+// v * 2^e exactly (two steps keep each factor a normal fp32).
+__device__ __forceinline__ float mul_pow2(float v, int e) {
+  int e1 = e > 126 ? 126 : (e < -126 ? -126 : e);
+  int e2 = e - e1;
+  v = __fmul_rn(v, __int_as_float((e1 + 127) << 23));
+  if (e2 != 0) v = __fmul_rn(v, __int_as_float((max(min(e2, 126), -126) + 127) << 23));
+  return v;
+}
+
+// Offset (in f16) of the 8 activations starting at staged column e: tile
+// e/128, 32-column chunk c, 8-column sub-block q.  Chunks 2 and 3 store
+// their sub-blocks in XOR-2 order so the four chunks a warp reads at once
+// fall in distinct shared-memory banks.
+__device__ __forceinline__ int x_off(int e) {
+  const int c = (e >> 5) & 3, q = (e >> 3) & 3;
+  return (e >> 7) * kTileHalves + c * 32 + ((q ^ (c & 2)) << 3);
+}
+
+__device__ __forceinline__ uint4 scale_to_f16(uint4 q, int sh) {
+  uint4 h;
+  h.x = f32x2_to_f16x2(mul_pow2(bf16_hi(q.x), sh), mul_pow2(bf16_lo(q.x), sh));
+  h.y = f32x2_to_f16x2(mul_pow2(bf16_hi(q.y), sh), mul_pow2(bf16_lo(q.y), sh));
+  h.z = f32x2_to_f16x2(mul_pow2(bf16_hi(q.z), sh), mul_pow2(bf16_lo(q.z), sh));
+  h.w = f32x2_to_f16x2(mul_pow2(bf16_hi(q.w), sh), mul_pow2(bf16_lo(q.w), sh));
+  return h;
+}
+
+__device__ __forceinline__ uint32_t absmax8(uint32_t mx, uint4 q) {
+  mx = __vmaxu2(mx, q.x & 0x7FFF7FFFu);
+  mx = __vmaxu2(mx, q.y & 0x7FFF7FFFu);
+  mx = __vmaxu2(mx, q.z & 0x7FFF7FFFu);
+  mx = __vmaxu2(mx, q.w & 0x7FFF7FFFu);
+  return mx;
+}
+
+// D += A * B with A 16x16 f16 (row), B 16x8 f16 (col), fp32 accumulate.
+// Not volatile: the compiler may interleave independent MMA chains.
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One unit of one warp: both k-tiles, MMAs of the two tiles interleaved.
+// wlo/whi: the lane's 16 nibble bytes of rows g / g+8 per tile; sw: the
+// lane's scale word per tile (rows g, g+8 x blocks 2c, 2c+1); xr: the
+// lane's 32 activations per tile and n8 block of tokens, as f16 pairs.
+template <int NT>
+__device__ __forceinline__ void unit_mma(float (&acc)[2][NT][4], const uint4 (&wlo)[2],
+                                         const uint4 (&whi)[2], const uint32_t (&sw)[2],
+                                         const uint32_t (&xr)[2][NT][16]) {
+  uint32_t sa[2][2], sb[2][2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const uint32_t s01 = e4m3x2_to_f16x2(uint16_t(sw[t] & 0xFFFFu));
+    const uint32_t s23 = e4m3x2_to_f16x2(uint16_t(sw[t] >> 16));
+    sa[t][0] = __byte_perm(s01, 0, 0x1010);
+    sa[t][1] = __byte_perm(s01, 0, 0x3232);
+    sb[t][0] = __byte_perm(s23, 0, 0x1010);
+    sb[t][1] = __byte_perm(s23, 0, 0x3232);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t fl[2][4], fh[2][4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t lo = q == 0 ? wlo[t].x : q == 1 ? wlo[t].y : q == 2 ? wlo[t].z : wlo[t].w;
+      const uint32_t hi = q == 0 ? whi[t].x : q == 1 ? whi[t].y : q == 2 ? whi[t].z : whi[t].w;
+      e2m1x8_to_f16x2x4(lo, fl[t]);
+      e2m1x8_to_f16x2x4(hi, fh[t]);
+    }
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int s = 2 * q + h;
+      uint32_t A[2][4];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        A[t][0] = hmul2(fl[t][2 * h], sa[t][q >> 1]);
+        A[t][1] = hmul2(fh[t][2 * h], sb[t][q >> 1]);
+        A[t][2] = hmul2(fl[t][2 * h + 1], sa[t][q >> 1]);
+        A[t][3] = hmul2(fh[t][2 * h + 1], sb[t][q >> 1]);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int t = 0; t < 2; ++t) mma_f16(acc[t][nt], A[t], xr[t][nt][2 * s], xr[t][nt][2 * s + 1]);
+    }
+  }
+}
+
+// Producer: stream this CTA's units of projection p into the ring.  j
+// numbers the units this CTA handles across every projection of the launch,
+// in the same order the consumers take them.  Returns false after a
+// bounded wait gave up (the CTA is then aborting).
+__device__ __forceinline__ bool produce(const Proj &p, uint8_t *base, Ctrl &ct, int S,
+                                        RingPos &pos, volatile int *aborted, unsigned *status) {
+  const int64_t grid = p.grid;
+  if (int64_t(blockIdx.x) >= grid) return true;
+  const int64_t u_begin = range_begin(blockIdx.x, p.total, grid);
+  const int64_t u_end = range_begin(blockIdx.x + 1, p.total, grid);
+  for (int64_t u = u_begin; u < u_end; ++u, pos.advance(S)) {
+    const int st = pos.st;
+    // the stage was last filled one pass ago: wait for its release
+    if (pos.wrapped && !mbar_wait(&ct.empty[st], pos.phase ^ 1u, aborted)) {
+      if (!*aborted) {
+        *aborted = 1;
+        raise_status(status, kDevTimeout);
+      }
+      return false;
+    }
+    if (*aborted) return false;
+    const int64_t rb = u / p.units;
+    const int uk = int(u - rb * p.units);
+    uint8_t *stage = base + st * kStageBytes;
+    mbar_expect_tx(&ct.full[st], kStageBytes);
+    tma_load_2d(stage, p.tm_w, uk * kUnitCols, int(rb * kRB), &ct.full[st]);
+    tma_load_2d(stage + kPackedStage, p.tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[st]);
+  }
+  return true;
+}
+
+// No copy may still be landing in shared memory when the CTA exits: wait
+// (bounded) for the last phase of every stage that was filled.  `issued`
+// counts the units whose copies were started.
+__device__ __forceinline__ void drain(Ctrl &ct, int S, int64_t issued) {
+  int never = 0;
+  for (int64_t j = issued > S ? issued - S : 0; j < issued; ++j)
+    mbar_wait(&ct.full[j % S], unsigned(j / S) & 1u, &never);
+}
+
+// Consumers: the whole of this CTA's share of projection p -- activation
+// staging, the unit loop, and the split-K epilogue.  Called by the kW
+// consumer warps only.
+template <int NT>
+__device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *base, Ctrl &ct,
+                                        uint16_t *xs, RingPos &pos, volatile int *aborted) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int rg = warp;
+  const int64_t grid = p.grid;
+  if (int64_t(blockIdx.x) >= grid) return;
+  const int64_t u_begin = range_begin(blockIdx.x, p.total, grid);
+  const int64_t u_end = range_begin(blockIdx.x + 1, p.total, grid);
+  if (u_begin >= u_end) return;
+  const int S = r.stages, m = r.m, units = p.units;
+
+  // 128-byte swizzle: logical 16-byte chunk ch of box row r sits at ch ^ (r & 7);
+  // rows rg*16 + g and rg*16 + g + 8 both have r & 7 == g.
+  int off_lo[2], off_hi[2], off_sc[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    off_lo[t] = (rg * 16 + g) * kUnitCols + (((t * 4 + c) ^ g) << 4);
+    off_hi[t] = (rg * 16 + g + 8) * kUnitCols + (((t * 4 + c) ^ g) << 4);
+    off_sc[t] = kPackedStage + rg * (kKT * 128) + t * 128 + lane * 4;
+  }
+
+  // -- which k-units this CTA touches: all of them when its range covers a
+  //    row block, else the L consecutive units (mod units) from uk_begin
+  const int64_t L = u_end - u_begin;
+  const bool all_units = L >= units;
+  const int uk_begin = int(u_begin % units);
+  const int slots = x_slots(L, units);
+  const bool full = int64_t(m) * x_stride_full(slots) <= r.x_cap;
+  const int stride = full ? x_stride_full(slots) : x_stride_chunk(m);
+
+  // -- per-token power-of-two shift from the largest |x| over the staged
+  //    columns (a function of the token's own data and the partition only,
+  //    never of m); in full mode the raw bf16 values land in shared memory
+  //    on the same pass and are converted in place afterwards.
+  if (threadIdx.x < 16) ct.xmax[threadIdx.x] = 0;
+  consumer_sync();
+  {
+    const int nv = slots * (kUnitK / 8);
+    for (int tok = 0; tok < m; ++tok) {
+      const uint16_t *xrow = p.x + int64_t(tok) * p.k;
+      uint32_t mx = 0;
+      for (int v = threadIdx.x; v < nv; v += kW * 32) {
+        const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
+        const int uk = all_units ? s : (uk_begin + s) % units;
+        const int kk = uk * kUnitK + within;
+        uint4 q = make_uint4(0, 0, 0, 0);
+        if (kk < p.k) q = __ldg(reinterpret_cast<const uint4 *>(xrow + kk));
+        mx = absmax8(mx, q);
+        if (full) *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) = q;
+      }
+      mx = max(mx & 0xFFFFu, mx >> 16);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+      if (lane == 0 && mx != 0) atomicMax(&ct.xmax[tok], mx);
+    }
+  }
+  consumer_sync();
+  if (threadIdx.x < m) {
+    const uint32_t b = ct.xmax[threadIdx.x];
+    int sh = 0;
+    if (b != 0 && b < 0x7F80u) sh = 14 - ilogbf(__uint_as_float(b << 16));
+    ct.shift[threadIdx.x] = sh;
+  }
+  consumer_sync();
+  if (full) {
+    const int nv = slots * (kUnitK / 8);
+    for (int tok = 0; tok < m; ++tok) {
+      const int sh = ct.shift[tok];
+      for (int v = threadIdx.x; v < nv; v += kW * 32) {
+        uint4 *q = reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8));
+        *q = scale_to_f16(*q, sh);  // written by this same thread above
+      }
+    }
+    consumer_sync();
+  }
+  const float gd = __ldg(p.g_dec);
+
+  int64_t u = u_begin;
+  while (u < u_end) {
+    const int64_t rb = u / units;
+    const int uk0 = int(u - rb * units);
+    const int uk1 = int(uk0 + (u_end - u) < units ? uk0 + (u_end - u) : units);
+
+    float acc[2][NT][4];
+#pragma unroll
+    for (int t = 0; t < 2; ++t)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[t][nt][i] = 0.0f;
+
+    const int step_units = full ? (uk1 - uk0) : chunk_units_for(m);
+    for (int cu0 = uk0; cu0 < uk1; cu0 += step_units) {
+      const int cu1 = min(uk1, cu0 + step_units);
+      if (!full) {
+        consumer_sync();  // earlier readers of the staging buffer are done
+        const int nv = (cu1 - cu0) * (kUnitK / 8);
+        for (int idx = threadIdx.x; idx < m * nv; idx += kW * 32) {
+          const int tok = idx / nv, v = idx - tok * nv;
+          const int kk = cu0 * kUnitK + v * 8;
+          uint4 q = make_uint4(0, 0, 0, 0);
+          if (kk < p.k) q = __ldg(reinterpret_cast<const uint4 *>(p.x + int64_t(tok) * p.k + kk));
+          *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) =
+              scale_to_f16(q, ct.shift[tok]);
+        }
+        consumer_sync();
+      }
+
+      // staged slot of unit cu0 (slots follow units, wrapping at `units`)
+      int slot = full ? (all_units ? cu0 : (cu0 >= uk_begin ? cu0 - uk_begin : cu0 + units - uk_begin))
+                      : 0;
+      for (int uk = cu0; uk < cu1; ++uk, ++slot, pos.advance(S)) {
+        const int st = pos.st;
+        uint4 wlo[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        uint4 whi[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+        uint32_t sw[2] = {0, 0};
+        const bool ok = !*aborted && mbar_wait(&ct.full[st], pos.phase, aborted);
+        if (ok) {
+          const uint8_t *stage = base + st * kStageBytes;
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            wlo[t] = *reinterpret_cast<const uint4 *>(stage + off_lo[t]);
+            whi[t] = *reinterpret_cast<const uint4 *>(stage + off_hi[t]);
+            sw[t] = *reinterpret_cast<const uint32_t *>(stage + off_sc[t]);
+          }
+        } else if (lane == 0 && !*aborted) {
+          *aborted = 1;
+          raise_status(r.status, kDevTimeout);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ct.empty[st]);
+
+        // -- activations of the unit's two k-tiles for each n8 block of tokens
+        uint32_t xr[2][NT][16];
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int tl = slot * kKT + t;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const int tok = min(nt * 8 + g, m - 1);
+            const uint4 *px =
+                reinterpret_cast<const uint4 *>(xs + tok * stride + tl * kTileHalves + 32 * c);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 v = px[q ^ (c & 2)];
+              xr[t][nt][4 * q + 0] = v.x;
+              xr[t][nt][4 * q + 1] = v.y;
+              xr[t][nt][4 * q + 2] = v.z;
+              xr[t][nt][4 * q + 3] = v.w;
+            }
+          }
+        }
+        unit_mma<NT>(acc, wlo, whi, sw, xr);
+      }
+    }
+
+    // -- epilogue: this warp holds rows g, g+8 x tokens nt*8 + 2c + {0,1};
+    //    the two k-tile accumulators are added in a fixed order
+    const bool complete = (uk0 == 0 && uk1 == units);
+    const int64_t unit0 = rb * units;
+    const int64_t own_lo = owner_of(unit0, p.total, grid);
+    const int contrib = int(owner_of(unit0 + units - 1, p.total, grid) - own_lo + 1);
+    const int jj = int(blockIdx.x - own_lo);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int token = nt * 8 + 2 * c + (i & 1);
+        const int row_local = rg * 16 + g + 8 * (i >> 1);
+        if (token >= m) continue;
+        const float v = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[token]);
+        if (complete) {
+          const int64_t row = rb * kRB + row_local;
+          if (row < p.n) p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(v, gd));
+        } else {
+          r.partial[((rb * p.max_contrib + jj) * kRB + row_local) * 16 + token] = v;
+        }
+      }
+    if (!complete) {
+      // the barrier orders every warp's partial stores before thread 0's
+      // gpu-scope fence, which publishes them with the ticket increment
+      consumer_sync();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned ticket = atomicAdd(&r.tickets[rb], 1u);
+        __threadfence();
+        ct.flag = (ticket == unsigned(contrib - 1));
+      }
+      consumer_sync();
+      if (ct.flag) {
+        for (int idx = threadIdx.x; idx < kRB * m; idx += kW * 32) {
+          const int row_local = idx / m, token = idx - row_local * m;
+          const int64_t row = rb * kRB + row_local;
+          if (row >= p.n) continue;
+          float s = 0.0f;
+          for (int q = 0; q < contrib; ++q)
+            s = __fadd_rn(s, __ldcg(r.partial + ((rb * p.max_contrib + q) * kRB + row_local) * 16 +
+                                    token));
+          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(s, gd));
+        }
+        if (threadIdx.x == 0) r.tickets[rb] = 0;
+      }
+    }
+    u += uk1 - uk0;
+  }
+}
+
+// Shared-memory carve-up: ring (1 KiB aligned), control block, activations.
+struct SmemView {
+  uint8_t *base;
+  Ctrl *ct;
+  uint16_t *xs;
+};
+__device__ __forceinline__ SmemView carve(uint8_t *raw, int stages) {
+  SmemView v;
+  v.base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
+  v.ct = reinterpret_cast<Ctrl *>(v.base + stages * kStageBytes);
+  v.xs = reinterpret_cast<uint16_t *>(v.base + stages * kStageBytes + kCtrlBytes);
+  return v;
+}
+
+__device__ __forceinline__ void init_ring(Ctrl &ct, int S) {
+  for (int s = 0; s < S; ++s) {
+    mbar_init(&ct.full[s], 1);
+    mbar_init(&ct.empty[s], kW);
+  }
+  ct.aborted = 0;
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+#endif  // __CUDACC__
+
+// Host-side helpers shared by the launchers.
+size_t smem_bytes(int stages, int x_cap_halves);
+int stages_for(int x_cap_halves);
+bool encode_maps(const aq_nvfp4_weight &w, CUtensorMap *tm_w, CUtensorMap *tm_s);
+
+}  // namespace core
+}  // namespace aq

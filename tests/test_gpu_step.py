@@ -90,3 +90,80 @@ def test_full_1b_step_against_oracle():
         packed, scales, ge, gd = oracle.quantize(bits(Ws[i]))
         y_ref = oracle.gemv(packed, scales, gd, bits(xs[i]))
         assert_gemv_close(ys[i], y_ref, "projection %d" % i)
+
+
+# ------------------------------------------------------------ persistent step
+
+@pytest.mark.parametrize("m", [1, 3])
+def test_persistent_step_matches_oracle_and_separate_calls(m):
+    """One cooperative launch for the whole stack: every projection within
+    tolerance of the oracle, and of the per-projection launches."""
+    Ws, ws, xs, ys = build_stack(3, inputs.LAYER_1B, m, seed=11)
+    plan = aq.StepPlan(ws, xs, ys)
+    wsp = plan.workspace()
+    aq.step_run(plan, wsp)
+    torch.cuda.synchronize()
+    assert aq.poll_device_status() == aq.OK
+    for i, (W, w, x, y) in enumerate(zip(Ws, ws, xs, ys)):
+        packed, scales, ge, gd = oracle.quantize(bits(W))
+        y_ref = oracle.gemv(packed, scales, gd, bits(x))
+        assert_gemv_close(y, y_ref, "projection %d" % i)
+        assert_gemv_close(gemv_gpu(w, x), y_ref, "separate %d" % i)
+
+
+def test_persistent_step_repeats_bit_exact_and_is_m_invariant():
+    Ws, ws, xs4, ys4 = build_stack(2, inputs.LAYER_31B[:2], 4, seed=12)
+    plan4 = aq.StepPlan(ws, xs4, ys4)
+    wsp = plan4.workspace()
+    aq.step_run(plan4, wsp)
+    torch.cuda.synchronize()
+    first = [y.clone() for y in ys4]
+    aq.step_run(plan4, wsp)
+    torch.cuda.synchronize()
+    for a, b in zip(ys4, first):
+        assert torch.equal(a, b)
+    xs1 = [x[2:3].contiguous() for x in xs4]
+    ys1 = [torch.empty((1, y.shape[1]), dtype=torch.bfloat16, device=DEV) for y in ys4]
+    plan1 = aq.StepPlan(ws, xs1, ys1)
+    aq.step_run(plan1, plan1.workspace())
+    torch.cuda.synchronize()
+    for a, b in zip(ys1, first):
+        assert torch.equal(a[0], b[2])
+    assert aq.poll_device_status() == aq.OK
+
+
+def test_persistent_step_in_a_cuda_graph():
+    Ws, ws, xs, ys = build_stack(2, inputs.LAYER_1B, 1, seed=13)
+    plan = aq.StepPlan(ws, xs, ys)
+    wsp = plan.workspace()
+    aq.step_run(plan, wsp)
+    torch.cuda.synchronize()
+    eager = [y.clone() for y in ys]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        for y in ys:
+            y.zero_()
+        with torch.cuda.graph(graph, stream=side):
+            aq.step_run(plan, wsp, stream=side)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(ys, eager):
+        assert torch.equal(a, b)
+
+
+def test_persistent_step_rejects_mismatched_run_on_device():
+    """A run whose m or workspace does not match its plan launches, finds
+    the mismatch on the device before touching memory, and reports it."""
+    Ws, ws, xs, ys = build_stack(1, inputs.LAYER_1B, 1, seed=14)
+    plan = aq.StepPlan(ws, xs, ys)
+    wsp = plan.workspace()
+    aq.step_run(plan, wsp, m=2)
+    assert aq.poll_device_status() == aq.ERR_INVALID_ARG
+    small = torch.zeros(1024, dtype=torch.uint8, device=DEV)
+    aq.step_run(plan, small)
+    assert aq.poll_device_status() == aq.ERR_INVALID_ARG
+    aq.step_run(plan, wsp)
+    assert aq.poll_device_status() == aq.OK
