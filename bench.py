@@ -4,18 +4,20 @@ Workload (default): the ~31B-shaped decoder stack, 60 layers x {fused QKV
 [8192, 5376], o_proj [5376, 4096], fused gate+up [43008, 5376], down
 [5376, 21504]} in NVFP4 (13,934,592,000 bytes of weights, far larger than
 L2), one bf16 token per projection, all 240 projections streamed in order on
-one stream per step through aq_decode_step_weights (captured once in a CUDA
-graph, programmatic dependent launch between projections).  Weights are
-seeded synthetic N(0, 0.02^2) with 0.1% x20 outliers, quantised on the GPU
-by the library before timing.
+one stream per step: aq_decode_step_weights (one GEMV launch per fused
+projection, programmatic dependent launch between them) captured once in a
+CUDA graph and replayed.  Weights are seeded synthetic N(0, 0.02^2) with
+0.1% x20 outliers, quantised on the GPU by the library before timing.
 
 Metric: algorithmic HBM GB/s of the step (0.5625 B per weight element + 4 B
 per-tensor scale + activations in + outputs out) and ms per step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl aq|reference]
+                    [--workload 31b|1b] [--layers L] [--m M] [--no-extras]
 
 One JSON line is printed by rank 0.  With N > 1 (torchrun) every rank runs
 an independent replica on its own GPU (the path has no exchange step).
+``--layers`` streams only the first L layers (a small case for profilers).
 """
 import argparse
 import hashlib
@@ -33,10 +35,15 @@ sys.path.insert(0, ROOT)
 METRIC = "NVFP4 decode GEMV HBM GB/s (% of 8 TB/s); ms per 31B-shaped step weight stream"
 NOMINAL_HBM_GBS = 8000.0  # the 8 TB/s denominator the metric names
 
-# DRAM bytes per GEMV launch from one ncu capture (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by the sha1 of the kernel source it was
-# taken on; when gemv.cu changes the figure no longer applies (null).
-NCU_TRAFFIC = {}
+# DRAM bytes of one layer's GEMV launches (dram__bytes_read.sum +
+# dram__bytes_write.sum summed over the layer's four launches in one ncu
+# capture), keyed by the workload and the sha1 of the GEMV kernel sources the
+# capture was taken on; when they change the figure no longer applies (null).
+NCU_TRAFFIC = {
+    # four launches of layer 0, m = 1: 27,710,208 + 15,107,840 + 137,514,752
+    # + 67,917,056 bytes (profiles/gemv_kernel_31b_layer_dram_traffic.md)
+    ("gemma4-31b-shaped decode-step weight stream", 1, "37c718cca8f19dbbcadc602e257ce6ced50f1bab"): 248249856,
+}
 
 
 def parse():
@@ -47,6 +54,8 @@ def parse():
     p.add_argument("--impl", choices=("aq", "reference"), default="aq")
     p.add_argument("--m", type=int, default=1, help="tokens per projection")
     p.add_argument("--workload", choices=("31b", "1b"), default="31b")
+    p.add_argument("--layers", type=int, default=0,
+                   help="stream only the first L layers (0: all of the workload's layers)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the eager / no-PDL / end-to-end / CPU-baseline legs")
     return p.parse_args()
@@ -277,7 +286,7 @@ def time_region(run_step, steps, warmup, stream, dist, sampler=None):
 
 def kernel_sha():
     h = hashlib.sha1()
-    for name in ("gemv_core.cuh", "step.cu"):
+    for name in ("gemv_core.cuh", "gemv.cu"):
         h.update(open(os.path.join(ROOT, "nvfp4_block_scaled_aq_gb300", "csrc", name), "rb").read())
     return h.hexdigest()
 
@@ -336,6 +345,10 @@ def run_aq(a, dist):
     torch.cuda.set_device(dist.local)
     device = torch.device("cuda", dist.local)
     name, shapes, layers = workload(a.workload)
+    layer_traffic = NCU_TRAFFIC.get((name, a.m, kernel_sha()))
+    if a.layers:
+        layers = min(layers, a.layers)
+        name += " (first %d layers)" % layers
     stack = Stack(shapes, layers, a.m, device)
     step_bytes = algorithmic_bytes(shapes, layers, a.m)
     stream = torch.cuda.Stream(device)
@@ -349,9 +362,11 @@ def run_aq(a, dist):
     def persistent():
         aq.step_run(stack.plan, stack.plan_ws, stream=stream)
 
+    # the timed path: one GEMV launch per projection (PDL), captured in a graph
+    g_pdl = capture(stack, aq.STEP_PDL, stream)
     sampler = ClockSampler(dist.local) if dist.rank == 0 else None
     time.sleep(0.3 if sampler else 0)
-    secs = time_region(persistent, a.steps, a.warmup, stream, dist, sampler)
+    secs = time_region(replay(g_pdl), a.steps, a.warmup, stream, dist, sampler)
     if sampler:
         sampler.stop()
     ms = secs / a.steps * 1e3
@@ -360,10 +375,8 @@ def run_aq(a, dist):
     extras = {}
     e2e = None
     if not a.no_extras:
-        g_pdl = capture(stack, aq.STEP_PDL, stream)
-        extras["per_projection_graph_pdl_ms_per_step"] = round(
-            time_region(replay(g_pdl), a.steps, a.warmup, stream, dist) / a.steps * 1e3, 4)
-        del g_pdl
+        extras["persistent_step_run_ms_per_step"] = round(
+            time_region(persistent, a.steps, a.warmup, stream, dist) / a.steps * 1e3, 4)
         g_nopdl = capture(stack, 0, stream)
         extras["per_projection_graph_no_pdl_ms_per_step"] = round(
             time_region(replay(g_nopdl), a.steps, a.warmup, stream, dist) / a.steps * 1e3, 4)
@@ -383,7 +396,7 @@ def run_aq(a, dist):
         def e2e_step():
             with torch.cuda.stream(stream):
                 stack.x_all.copy_(x_host, non_blocking=True)
-                aq.step_run(stack.plan, stack.plan_ws, stream=stream)
+                g_pdl.replay()
                 y_host.copy_(stack.y_all, non_blocking=True)
         e2e_secs = time_region(e2e_step, a.steps, a.warmup, stream, dist)
         e2e = {"value": round(dist.world * step_bytes * a.steps / e2e_secs / 1e9, 2),
@@ -391,21 +404,25 @@ def run_aq(a, dist):
                "ms_per_step": round(e2e_secs / a.steps * 1e3, 4),
                "h2d_bytes_per_step": stack.x_all.numel() * 2,
                "d2h_bytes_per_step": stack.y_all.numel() * 2,
-               "path": "aq_step_run (one launch per step), pinned host buffers"}
+               "path": "aq_decode_step_weights graph replay, pinned host buffers copied "
+                       "in and out inside the timed region"}
+    del g_pdl
 
     st = aq.poll_device_status()
     if st != aq.OK:
         raise RuntimeError("device status %d after timing: %s" % (st, aq.last_error()))
 
     peak, peak_kind = load_peaks()
-    launch_bytes = step_bytes  # one persistent launch streams the whole step
-    launch_s = secs / a.steps
+    # the step is stack.launches GEMV launches; with PDL they overlap, so the
+    # average launch is the step's bytes and time divided by the launch count
+    launch_bytes = step_bytes / stack.launches
+    launch_s = secs / a.steps / stack.launches
     achieved = launch_bytes / launch_s / 1e9
-    traffic = NCU_TRAFFIC.get(kernel_sha())
+    traffic = None if layer_traffic is None else round(layer_traffic * layers / stack.launches)
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)",
-                "kernel": "step_kernel<1> (aq_step_run: all projections of the step)",
+                "kernel": "gemv_kernel<1> (aq_decode_step_weights: one launch per projection)",
                 "algorithmic_bytes_per_launch": round(launch_bytes)}
 
     cpu = None
@@ -424,14 +441,15 @@ def run_aq(a, dist):
                    "projections": [list(s) for s in shapes], "m": a.m,
                    "weight_bytes_per_step": weight_bytes(shapes, layers),
                    "algorithmic_bytes_per_step": step_bytes,
-                   "launch": "aq_step_run: one persistent cooperative launch per step",
+                   "launch": "aq_decode_step_weights (PDL) captured in one CUDA graph, "
+                             "%d GEMV launches per step" % stack.launches,
                    "l2": "inputs larger than L2 (weights %.1f GB per step)" %
                          (weight_bytes(shapes, layers) / 1e9),
                    "parallelism": "replicas x%d" % dist.world},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": a.steps,
+        "gpu_launches": a.steps * stack.launches,
         "clocks": clocks,
         "extras": extras,
     }
