@@ -170,6 +170,31 @@ AQ_API aq_status aq_gemv_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int3
                         uint16_t *y, aq_path path, void *workspace,
                         size_t workspace_bytes, aq_stream_t stream);
 
+/* aq_gemv_nvfp4 without a workspace argument, for callers that cannot
+ * allocate device memory: a plugin inside a host program that owns every
+ * device allocation and forbids cudaMalloc once it is serving (cudaMalloc
+ * may synchronise the device), or a binding that can pass buffers but not
+ * create them.  The pages have no counterpart of this call; it exists for
+ * such callers only.
+ *
+ * Arguments, results and errors are those of aq_gemv_nvfp4.  The split-K
+ * scratch is a fixed array of AQ_GEMV_NOALLOC_MAX_SCRATCH bytes inside the
+ * library, in device memory, which every GPU that loads the library holds
+ * until the process exits; nothing is allocated, on the device or the host.
+ * A weight whose scratch (aq_gemv_workspace_bytes(n, k, m) on the current
+ * device) exceeds that size is rejected with AQ_ERR_WORKSPACE before any
+ * launch.  The first call on each device sets the array up synchronously
+ * (looks up its address and zero-fills it), so that first call must come
+ * before any stream capture.  Every call then clears, on `stream`, the
+ * part of the array that has to start at zero, and launches the GEMV.
+ * All calls on a device share the one array, which keeps the last call's
+ * contents: calls whose kernels can overlap on the GPU (different streams,
+ * different host threads) race on it and must be ordered by the caller. */
+#define AQ_GEMV_NOALLOC_MAX_SCRATCH (8u << 20) /* bytes per device */
+AQ_API aq_status aq_gemv_nvfp4_noalloc(const aq_nvfp4_weight *w, const uint16_t *x,
+                                       int32_t m, uint16_t *y, aq_path path,
+                                       aq_stream_t stream);
+
 /* Flags of aq_decode_step_weights. */
 #define AQ_STEP_PDL 1u /* programmatic dependent launch between projections */
 

@@ -30,6 +30,7 @@ STATUS_NAMES = {0: "AQ_OK", 1: "AQ_ERR_INVALID_ARG", 2: "AQ_ERR_SHAPE",
 PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
 STEP_PDL = 1
 MAX_M = 16
+NOALLOC_MAX_SCRATCH = 8 << 20  # AQ_GEMV_NOALLOC_MAX_SCRATCH
 
 
 class AqLibraryMissing(RuntimeError):
@@ -81,6 +82,7 @@ def _declare(L):
                                            _sz, _p], C.c_int),
         "aq_gemv_workspace_bytes": ([_i32, _i32, _i32], _sz),
         "aq_gemv_nvfp4": ([W, _p, _i32, _p, C.c_int, _p, _sz, _p], C.c_int),
+        "aq_gemv_nvfp4_noalloc": ([W, _p, _i32, _p, C.c_int, _p], C.c_int),
         "aq_decode_step_weights": ([W, _i32, C.POINTER(_p), C.POINTER(_p), _i32,
                                     C.c_uint32, _p, _sz, _p], C.c_int),
         "aq_scales_to_canonical": ([W, _p, _p], C.c_int),
@@ -199,6 +201,14 @@ def gemv(w: Nvfp4Weight, x, y, workspace, path=PATH_AUTO, stream=None):
     check(lib().aq_gemv_nvfp4(C.byref(wc), _ptr(x), m, _ptr(y), path, _ptr(workspace),
                               workspace.numel() * workspace.element_size(),
                               _stream(stream)))
+
+
+def gemv_noalloc(w: Nvfp4Weight, x, y, path=PATH_AUTO, stream=None):
+    """aq_gemv_nvfp4 with the library's own fixed scratch (no workspace)."""
+    m = x.shape[0]
+    wc = w.c()
+    check(lib().aq_gemv_nvfp4_noalloc(C.byref(wc), _ptr(x), m, _ptr(y), path,
+                                      _stream(stream)))
 
 
 class StepArgs:

@@ -221,7 +221,7 @@ size_t aq_gemv_workspace_bytes(int32_t n, int32_t k, int32_t m) {
 }
 
 // Host-only checks of one GEMV call (no device query).
-static aq_status gemv_args(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m,
+aq_status gemv_args(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m,
                            const uint16_t *y, aq_path path, const char *what) {
   aq_status s = check_weight(w, what);
   if (s != AQ_OK) return s;

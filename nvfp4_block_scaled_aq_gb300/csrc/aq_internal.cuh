@@ -195,6 +195,9 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev);
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev);
 cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
                         void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st);
+cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, int m,
+                                 uint16_t *y, void *ws, const DeviceInfo &dev,
+                                 cudaStream_t st);
 
 size_t step_plan_bytes(int n_proj);
 aq_status step_plan_create(const aq_nvfp4_weight *w, int n_proj, const uint16_t *const *x,
@@ -204,3 +207,7 @@ cudaError_t launch_step(const void *plan, int m, void *ws, size_t ws_bytes, cons
                         cudaStream_t st);
 
 }  // namespace aq
+
+// Host-only checks of one GEMV call's arguments (api.cu).
+extern "C" aq_status gemv_args(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m, const uint16_t *y,
+                    aq_path path, const char *what);

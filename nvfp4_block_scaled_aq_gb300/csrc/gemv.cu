@@ -275,4 +275,58 @@ cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint
   return e;
 }
 
+// The same launch with both tensor maps encoded on the stack for this call
+// only (no map cache, so nothing is allocated on the host either) and
+// without programmatic dependent launch; ws is the caller's scratch.
+cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, int m,
+                                 uint16_t *y, void *ws, const DeviceInfo &dev,
+                                 cudaStream_t st) {
+  const GemvPlan plan = plan_gemv(w.n, w.k, dev);
+  CUtensorMap tm_w, tm_s;
+  if (!encoder()) return cudaErrorInvalidValue;
+  if (!make_map(&tm_w, w.packed, uint64_t(w.k) / 2, uint64_t(w.n), kUnitCols, kRB, true))
+    return cudaErrorInvalidValue;
+  const uint64_t srow = uint64_t(ceil_div(w.k, kTileCols)) * 128;
+  if (!make_map(&tm_s, w.scales, srow, uint64_t(ceil_div(w.n, kTileRows)), kKT * 128, kRG, false))
+    return cudaErrorInvalidValue;
+
+  Run r;
+  uint8_t *wsb = static_cast<uint8_t *>(ws);
+  r.tickets = reinterpret_cast<uint32_t *>(wsb);
+  r.partial = reinterpret_cast<float *>(wsb + kTicketBytes);
+  r.status = dev.status;
+  r.m = m;
+  r.x_cap = x_cap_for(plan, m);
+  r.stages = stages_for(r.x_cap);
+  if (r.stages < kMinStages) return cudaErrorInvalidConfiguration;
+
+  Proj p;
+  p.tm_w = nullptr;  // set from the kernel's own parameters
+  p.tm_s = nullptr;
+  p.g_dec = w.global_scale;
+  p.x = x;
+  p.y = y;
+  p.total = plan.total;
+  p.n = w.n;
+  p.k = w.k;
+  p.units = int(plan.units);
+  p.max_contrib = plan.max_contrib;
+  p.grid = plan.grid;
+
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes(r.stages, r.x_cap);
+  cfg.stream = st;
+  cudaError_t e;
+  if (m <= 8) {
+    if ((e = set_smem_attr<1>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1>, tm_w, tm_s, p, r);
+  } else {
+    if ((e = set_smem_attr<2>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2>, tm_w, tm_s, p, r);
+  }
+  return e;
+}
+
 }  // namespace aq
