@@ -145,11 +145,22 @@ AQ_API aq_status aq_reconstruct_quantize_nvfp4(const uint16_t *W0, const float *
                                         void *workspace, size_t workspace_bytes,
                                         aq_stream_t stream);
 
-/* GEMV paths. */
+/* GEMV paths.  AQ_PATH_GEMV keeps the bf16 activations at full precision
+ * and runs one of two kernels: the register-decode kernel (nibbles and
+ * scales dequantised to f16 in registers, mma.sync), or for 1..5 tokens the
+ * tcgen05 kernel, which hands the packed nibbles and E4M3 scales to the
+ * block-scaled fp4 MMA unchanged and gives it each token's activations as
+ * an exact-to-about-2^-19 sum of six NVFP4 terms.  AQ_PATH_AUTO and
+ * AQ_PATH_GEMV pick the faster kernel for the shape (today the
+ * register-decode one); the explicit choices exist for testing and
+ * measurement. */
 typedef enum {
-  AQ_PATH_AUTO = 0, /* choose by m                                       */
-  AQ_PATH_GEMV = 1, /* bf16 activations, weight dequantised in registers */
-  AQ_PATH_MMA = 2   /* activations quantised to NVFP4, tcgen05 MMA       */
+  AQ_PATH_AUTO = 0,           /* choose by m                                 */
+  AQ_PATH_GEMV = 1,           /* bf16 activations, kernel chosen by m        */
+  AQ_PATH_MMA = 2,            /* activations quantised to NVFP4, tcgen05 MMA */
+  AQ_PATH_GEMV_REGDECODE = 3, /* bf16 activations, register-decode kernel    */
+  AQ_PATH_GEMV_TCGEN05 = 4    /* bf16 activations, tcgen05 kernel (m <= 5;
+                                 AQ_ERR_UNSUPPORTED where it does not fit)  */
 } aq_path;
 
 /* Workspace of aq_gemv_nvfp4 / aq_decode_step_weights for a weight of
@@ -161,11 +172,14 @@ typedef enum {
 AQ_API size_t aq_gemv_workspace_bytes(int32_t n, int32_t k, int32_t m);
 
 /* y[t, i] = bf16( sum_k x[t, k] * w_hat[i, k] ), w_hat = e2m1(q)*sd*g_dec,
- * fp32 accumulation ("Future work": dequantise in registers).  x [m, k]
+ * fp32 accumulation ("Future work": a 4-bit GEMV at HBM bandwidth).  x [m, k]
  * bf16 and y [m, n] bf16 row-major, 16-byte aligned, y not overlapping x.
- * The result does not depend on m (each token's output equals the m = 1
- * call bit for bit) nor on timing: the split over the K axis is fixed by
- * (n, k) and its partial sums are added in a fixed order. */
+ * The result does not depend on timing (the split over the K axis is fixed
+ * by (n, k) and its partial sums are added in a fixed order), and, within
+ * one kernel, not on m: each token's output equals its m = 1 call bit for
+ * bit for every m the kernel serves (1..5 on the tcgen05 kernel, 1..16 on
+ * the register-decode kernel).  Both kernels meet the same tolerance
+ * against the exact product. */
 AQ_API aq_status aq_gemv_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m,
                         uint16_t *y, aq_path path, void *workspace,
                         size_t workspace_bytes, aq_stream_t stream);
@@ -177,7 +191,10 @@ AQ_API aq_status aq_gemv_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int3
  * create them.  The pages have no counterpart of this call; it exists for
  * such callers only.
  *
- * Arguments, results and errors are those of aq_gemv_nvfp4.  The split-K
+ * Arguments, results and errors are those of aq_gemv_nvfp4, computed by
+ * the register-decode kernel whatever m is: outputs equal aq_gemv_nvfp4
+ * with AQ_PATH_GEMV_REGDECODE bit for bit (AQ_PATH_GEMV_TCGEN05 is
+ * rejected with AQ_ERR_UNSUPPORTED).  The split-K
  * scratch is a fixed array of AQ_GEMV_NOALLOC_MAX_SCRATCH bytes inside the
  * library, in device memory, which every GPU that loads the library holds
  * until the process exits; nothing is allocated, on the device or the host.

@@ -27,7 +27,7 @@ STATUS_NAMES = {0: "AQ_OK", 1: "AQ_ERR_INVALID_ARG", 2: "AQ_ERR_SHAPE",
                 3: "AQ_ERR_ALIGNMENT", 4: "AQ_ERR_RANGE", 5: "AQ_ERR_UNSUPPORTED",
                 6: "AQ_ERR_TIMEOUT", 7: "AQ_ERR_CUDA", 8: "AQ_ERR_WORKSPACE"}
 
-PATH_AUTO, PATH_GEMV, PATH_MMA = 0, 1, 2
+PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_GEMV_REGDECODE, PATH_GEMV_TCGEN05 = 0, 1, 2, 3, 4
 STEP_PDL = 1
 MAX_M = 16
 NOALLOC_MAX_SCRATCH = 8 << 20  # AQ_GEMV_NOALLOC_MAX_SCRATCH

@@ -229,7 +229,8 @@ aq_status gemv_args(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m,
     return set_error(AQ_ERR_SHAPE, "%s: m = %d outside [1, %d]", what, m, AQ_MAX_M);
   if (path == AQ_PATH_MMA)
     return set_error(AQ_ERR_UNSUPPORTED, "%s: the MMA path is not built in this version", what);
-  if (path != AQ_PATH_AUTO && path != AQ_PATH_GEMV)
+  if (path != AQ_PATH_AUTO && path != AQ_PATH_GEMV && path != AQ_PATH_GEMV_REGDECODE &&
+      path != AQ_PATH_GEMV_TCGEN05)
     return set_error(AQ_ERR_INVALID_ARG, "%s: unknown path %d", what, int(path));
   if (!x || !y) return set_error(AQ_ERR_INVALID_ARG, "%s: x and y must not be NULL", what);
   if (!aligned(x, 16) || !aligned(y, 16))
@@ -247,9 +248,17 @@ aq_status aq_gemv_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m, 
   if (!dev) return AQ_ERR_UNSUPPORTED;
   if ((s = check_ws(workspace, workspace_bytes, gemv_workspace_bytes(w->n, w->k, *dev), what)) != AQ_OK)
     return s;
-  return launched(launch_gemv(*w, x, m, y, workspace, false, *dev,
-                              reinterpret_cast<cudaStream_t>(stream)),
-                  what);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (path == AQ_PATH_GEMV_REGDECODE)
+    return launched(launch_gemv_regdecode(*w, x, m, y, workspace, false, *dev, st), what);
+  if (path == AQ_PATH_GEMV_TCGEN05) {
+    if (!tc_eligible(w->n, w->k, m, *dev))
+      return set_error(AQ_ERR_UNSUPPORTED,
+                       "%s: the tcgen05 kernel does not serve [%d, %d] with m = %d", what, w->n,
+                       w->k, m);
+    return launched(launch_gemv_tc(*w, x, m, y, workspace, false, *dev, st), what);
+  }
+  return launched(launch_gemv(*w, x, m, y, workspace, false, *dev, st), what);
 }
 
 aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,

@@ -195,6 +195,17 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev);
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev);
 cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
                         void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st);
+// The tcgen05 kernel (tc_gemv.cu): its plan, whether it serves a shape for
+// m tokens, its workspace, and its launch.
+GemvPlan plan_gemv_tc(int n, int k, const DeviceInfo &dev);
+bool tc_eligible(int n, int k, int m, const DeviceInfo &dev);
+size_t gemv_tc_workspace_bytes(int n, int k, const DeviceInfo &dev);
+cudaError_t launch_gemv_tc(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
+                           void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st);
+// Register-decode kernel only (gemv.cu).
+cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
+                                  uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
+                                  cudaStream_t st);
 cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                  uint16_t *y, void *ws, const DeviceInfo &dev,
                                  cudaStream_t st);

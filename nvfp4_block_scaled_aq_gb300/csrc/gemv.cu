@@ -220,13 +220,28 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev) {
   return p;
 }
 
+// Enough for either kernel, so one workspace serves every token count.
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev) {
   const GemvPlan p = plan_gemv(n, k, dev);
-  return kTicketBytes + size_t(p.row_blocks) * p.max_contrib * kRB * 16 * sizeof(float);
+  const size_t reg = kTicketBytes + size_t(p.row_blocks) * p.max_contrib * kRB * 16 * sizeof(float);
+  const size_t tc = gemv_tc_workspace_bytes(n, k, dev);
+  return reg > tc ? reg : tc;
 }
 
+// The GEMV for m tokens.  Both kernels meet the same tolerance; the
+// register-decode kernel is the faster one on the measured decode shapes
+// today, so it serves every m unless the tcgen05 kernel is asked for.
+constexpr bool kAutoPrefersTc = false;
 cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
                         void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st) {
+  if (kAutoPrefersTc && tc_eligible(w.n, w.k, m, dev))
+    return launch_gemv_tc(w, x, m, y, ws, pdl, dev, st);
+  return launch_gemv_regdecode(w, x, m, y, ws, pdl, dev, st);
+}
+
+cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
+                                  uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
+                                  cudaStream_t st) {
   const GemvPlan plan = plan_gemv(w.n, w.k, dev);
   CUtensorMap tm_w, tm_s;
   if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;

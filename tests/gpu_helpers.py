@@ -29,14 +29,18 @@ def quantize_gpu(W):
     return w
 
 
-def gemv_gpu(w, x, ws=None):
+def gemv_gpu(w, x, ws=None, path=None):
     m = x.shape[0]
     if ws is None:
         ws = torch.zeros(aq.gemv_workspace_bytes(w.n, w.k, m), dtype=torch.uint8,
                          device=x.device)
     y = torch.empty((m, w.n), dtype=torch.bfloat16, device=x.device)
-    aq.gemv(w, x, y, ws)
+    aq.gemv(w, x, y, ws, path=aq.PATH_AUTO if path is None else path)
     return y
+
+
+# The two GEMV kernels: the tcgen05 one serves 1..5 tokens.
+KERNELS = {"tcgen05": (aq.PATH_GEMV_TCGEN05, 5), "regdecode": (aq.PATH_GEMV_REGDECODE, 16)}
 
 
 def weight_bytes(w):

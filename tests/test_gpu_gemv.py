@@ -5,8 +5,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_helpers import (DEV, assert_gemv_close, assert_quantized_equal, bits, gemv_gpu,
-                         quantize_gpu, require_gpu, weight_bytes)
+from gpu_helpers import (DEV, KERNELS, assert_gemv_close, assert_quantized_equal, bits,
+                         gemv_gpu, quantize_gpu, require_gpu, weight_bytes)
 from nvfp4_block_scaled_aq_gb300 import aq, inputs
 
 pytestmark = pytest.mark.gpu
@@ -34,11 +34,16 @@ def oracle_y(W, x):
     (65, 4096, 1), (300, 160, 7),
 ])
 def test_gemv_matches_oracle(n, k, m):
+    """Both kernels, and the automatic choice, within tolerance."""
     W = inputs.weight(n, k, seed=1000 + n + k, device=DEV)
     x = inputs.tokens(m, k, seed=2000 + m, device=DEV)
     w = quantize_gpu(W)
-    y = gemv_gpu(w, x)
-    assert_gemv_close(y, oracle_y(W, x), "n=%d k=%d m=%d" % (n, k, m))
+    y_ref = oracle_y(W, x)
+    assert_gemv_close(gemv_gpu(w, x), y_ref, "auto n=%d k=%d m=%d" % (n, k, m))
+    for name, (path, max_m) in KERNELS.items():
+        if m <= max_m:
+            assert_gemv_close(gemv_gpu(w, x, path=path), y_ref,
+                              "%s n=%d k=%d m=%d" % (name, n, k, m))
     assert aq.poll_device_status() == aq.OK
 
 
@@ -56,17 +61,21 @@ def test_gemv_fused_qkv_config_exact_rounding_rate():
     assert exact > 0.98, exact
 
 
-def test_gemv_is_independent_of_m():
-    """Each token's output is bit-identical whatever else is in the batch."""
-    n, k = 1152, 6912
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+@pytest.mark.parametrize("n,k", [(1152, 6912), (13824, 1152)])
+def test_gemv_is_independent_of_m(kernel, n, k):
+    """On each kernel, each token's output is bit-identical whatever else
+    is in the batch."""
+    path, max_m = KERNELS[kernel]
     w = quantize_gpu(inputs.weight(n, k, seed=5, device=DEV))
-    x = inputs.tokens(16, k, seed=6, device=DEV)
-    y16 = gemv_gpu(w, x)
-    for m in (1, 3, 8, 9):
-        ym = gemv_gpu(w, x[:m].contiguous())
-        assert torch.equal(ym, y16[:m]), m
-    for t in (0, 7, 15):
-        assert torch.equal(gemv_gpu(w, x[t:t + 1].contiguous())[0], y16[t])
+    x = inputs.tokens(max_m, k, seed=6, device=DEV)
+    y_all = gemv_gpu(w, x, path=path)
+    for m in sorted({1, 2, 3, 8, 9, max_m}):
+        if m <= max_m:
+            ym = gemv_gpu(w, x[:m].contiguous(), path=path)
+            assert torch.equal(ym, y_all[:m]), m
+    for t in sorted({0, max_m // 2, max_m - 1}):
+        assert torch.equal(gemv_gpu(w, x[t:t + 1].contiguous(), path=path)[0], y_all[t])
 
 
 def test_gemv_is_deterministic_and_workspace_rearms():
@@ -95,30 +104,37 @@ def test_one_workspace_serves_interleaved_shapes():
             assert torch.equal(gemv_gpu(w, x, ws), want), i
 
 
-def test_gemv_power_of_two_input_scaling_is_exact():
-    """Scaling x by 2^j scales y by 2^j exactly: the kernel normalises the
-    activations by a power of two and undoes it exactly."""
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_gemv_power_of_two_input_scaling_is_exact(kernel):
+    """Scaling x by 2^j scales y by 2^j exactly: both kernels normalise the
+    activations by powers of two and undo them exactly."""
+    path = KERNELS[kernel][0]
     n, k = 300, 2048
     w = quantize_gpu(inputs.weight(n, k, seed=12, device=DEV))
     x = inputs.tokens(1, k, seed=13, device=DEV)
-    y = gemv_gpu(w, x).float()
+    y = gemv_gpu(w, x, path=path).float()
     for j in (-90, -20, 7, 60):
-        yj = gemv_gpu(w, (x.float() * 2.0 ** j).to(torch.bfloat16)).float()
+        yj = gemv_gpu(w, (x.float() * 2.0 ** j).to(torch.bfloat16), path=path).float()
         assert torch.equal(yj, y * 2.0 ** j), j
 
 
-def test_gemv_wide_dynamic_range_activations():
+@pytest.mark.parametrize("kernel", sorted(KERNELS))
+def test_gemv_wide_dynamic_range_activations(kernel):
     n, k = 128, 1024
     W = inputs.weight(n, k, seed=14, device=DEV)
     x = inputs.tokens(1, k, seed=15, device=DEV).float()
     x[0, ::7] *= 1e12
     x[0, 3::11] *= 1e-12
     x = x.to(torch.bfloat16)
-    y = gemv_gpu(quantize_gpu(W), x)
+    y = gemv_gpu(quantize_gpu(W), x, path=KERNELS[kernel][0])
     assert_gemv_close(y, oracle_y(W, x))
 
 
 def test_gemv_one_hot_tokens_return_columns():
+    """One-hot tokens give back columns of w_hat (bit-exact on the
+    register-decode kernel, whose f16 path is exact here; within tolerance
+    on the tcgen05 kernel, whose six-term activation sum is exact to about
+    2^-19)."""
     n, k = 64, 256
     W = inputs.weight(n, k, seed=16, device=DEV)
     w = quantize_gpu(W)
@@ -127,9 +143,12 @@ def test_gemv_one_hot_tokens_return_columns():
     x = torch.zeros((len(cols), k), dtype=torch.bfloat16, device=DEV)
     for t, c in enumerate(cols):
         x[t, c] = 1.0
-    y = gemv_gpu(w, x)
     y_ref = oracle.gemv(packed, scales, gd, bits(x))
+    y = gemv_gpu(w, x, path=aq.PATH_GEMV_REGDECODE)
     assert torch.equal(y.cpu(), torch.from_numpy(y_ref).to(torch.bfloat16))
+    for t0 in range(0, len(cols), 5):
+        xt = x[t0:t0 + 5].contiguous()
+        assert_gemv_close(gemv_gpu(w, xt, path=aq.PATH_GEMV_TCGEN05), y_ref[t0:t0 + 5])
 
 
 def test_passthrough_gemv_equals_plain_gemv_bit_exact():

@@ -37,7 +37,9 @@ def test_noalloc_matches_workspace_gemv_on_consecutive_calls():
         x = inputs.tokens(m, k, seed=seed + 100, device=DEV)
         ws_.append(w)
         xs.append(x)
-        refs.append(gemv_gpu(w, x))  # the existing entry point, own workspace
+        # the existing entry point, own workspace, on the kernel this entry
+        # point runs (the register-decode kernel)
+        refs.append(gemv_gpu(w, x, path=aq.PATH_GEMV_REGDECODE))
         outs.append(torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV))
     torch.cuda.synchronize()
     for rep in range(2):
