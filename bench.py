@@ -364,8 +364,17 @@ def run_aq(a, dist):
     def persistent():
         aq.step_run(stack.plan, stack.plan_ws, stream=stream)
 
-    # the timed path: one GEMV launch per projection (PDL), captured in a graph
-    g_pdl = capture(stack, aq.STEP_PDL, stream)
+    # the timed path: one GEMV launch per projection (PDL), captured in a
+    # graph, on the kernel that is faster for this stack (both are timed)
+    kernel_ms = {}
+    for kname, kflag in (("regdecode", aq.STEP_REGDECODE), ("tcgen05", aq.STEP_TCGEN05)):
+        g = capture(stack, aq.STEP_PDL | kflag, stream)
+        kernel_ms[kname] = time_region(replay(g), max(3, a.steps // 4), a.warmup, stream, dist) \
+            / max(3, a.steps // 4) * 1e3
+        del g
+    kernel = min(kernel_ms, key=kernel_ms.get)
+    kflag = aq.STEP_REGDECODE if kernel == "regdecode" else aq.STEP_TCGEN05
+    g_pdl = capture(stack, aq.STEP_PDL | kflag, stream)
     sampler = ClockSampler(dist.local) if dist.rank == 0 else None
     time.sleep(0.3 if sampler else 0)
     secs = time_region(replay(g_pdl), a.steps, a.warmup, stream, dist, sampler)
@@ -374,18 +383,19 @@ def run_aq(a, dist):
     ms = secs / a.steps * 1e3
     value = dist.world * step_bytes * a.steps / secs / 1e9
 
-    extras = {}
+    extras = {"kernel": kernel,
+              "graph_pdl_ms_per_step_by_kernel": {k: round(v, 4) for k, v in kernel_ms.items()}}
     e2e = None
     if not a.no_extras:
         extras["persistent_step_run_ms_per_step"] = round(
             time_region(persistent, a.steps, a.warmup, stream, dist) / a.steps * 1e3, 4)
-        g_nopdl = capture(stack, 0, stream)
+        g_nopdl = capture(stack, kflag, stream)
         extras["per_projection_graph_no_pdl_ms_per_step"] = round(
             time_region(replay(g_nopdl), a.steps, a.warmup, stream, dist) / a.steps * 1e3, 4)
         del g_nopdl
 
         def eager():
-            aq.decode_step(stack.args, stack.ws, flags=aq.STEP_PDL, stream=stream)
+            aq.decode_step(stack.args, stack.ws, flags=aq.STEP_PDL | kflag, stream=stream)
         with torch.cuda.stream(stream):
             extras["per_projection_eager_pdl_ms_per_step"] = round(
                 time_region(eager, a.steps, a.warmup, stream, dist) / a.steps * 1e3, 4)
@@ -420,11 +430,14 @@ def run_aq(a, dist):
     launch_bytes = step_bytes / stack.launches
     launch_s = secs / a.steps / stack.launches
     achieved = launch_bytes / launch_s / 1e9
+    if kernel != "regdecode":
+        layer_traffic = None  # the capture was of the register-decode kernel
     traffic = None if layer_traffic is None else round(layer_traffic * layers / stack.launches)
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)",
-                "kernel": "gemv_kernel<1> (aq_decode_step_weights: one launch per projection)",
+                "kernel": ("gemv_kernel<1>" if kernel == "regdecode" else "tc_gemv_kernel") +
+                          " (aq_decode_step_weights: one launch per projection)",
                 "algorithmic_bytes_per_launch": round(launch_bytes)}
 
     cpu = None

@@ -29,6 +29,8 @@ STATUS_NAMES = {0: "AQ_OK", 1: "AQ_ERR_INVALID_ARG", 2: "AQ_ERR_SHAPE",
 
 PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_GEMV_REGDECODE, PATH_GEMV_TCGEN05 = 0, 1, 2, 3, 4
 STEP_PDL = 1
+STEP_REGDECODE = 2
+STEP_TCGEN05 = 4
 MAX_M = 16
 NOALLOC_MAX_SCRATCH = 8 << 20  # AQ_GEMV_NOALLOC_MAX_SCRATCH
 

@@ -269,8 +269,10 @@ aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,
   if (n_proj < 0) return set_error(AQ_ERR_INVALID_ARG, "%s: n_proj < 0", what);
   if (n_proj == 0) return AQ_OK;
   if (!w || !x || !y) return set_error(AQ_ERR_INVALID_ARG, "%s: w, x, y must not be NULL", what);
-  if (flags & ~AQ_STEP_PDL)
+  if (flags & ~(AQ_STEP_PDL | AQ_STEP_REGDECODE | AQ_STEP_TCGEN05))
     return set_error(AQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", what, flags);
+  if ((flags & AQ_STEP_REGDECODE) && (flags & AQ_STEP_TCGEN05))
+    return set_error(AQ_ERR_INVALID_ARG, "%s: at most one kernel flag", what);
   // Validate every projection before the first launch.
   for (int32_t p = 0; p < n_proj; ++p) {
     aq_status s = gemv_args(&w[p], x[p], m, y[p], AQ_PATH_GEMV, what);
@@ -290,7 +292,13 @@ aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool pdl = (flags & AQ_STEP_PDL) != 0;
   for (int32_t p = 0; p < n_proj; ++p) {
-    cudaError_t e = launch_gemv(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
+    cudaError_t e;
+    if (flags & AQ_STEP_REGDECODE)
+      e = launch_gemv_regdecode(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
+    else if ((flags & AQ_STEP_TCGEN05) && tc_eligible(w[p].n, w[p].k, m, *dev))
+      e = launch_gemv_tc(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
+    else
+      e = launch_gemv(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
     if (e != cudaSuccess) return cuda_error(e, what);
   }
   return AQ_OK;

@@ -63,11 +63,25 @@ constexpr int kTcMaxTokens = 5;
 constexpr int kTcThreads = 448;
 constexpr int kWarpMma = 1, kWarpEpi = 6;  // scale warps 2..5, staging-only warps 10..13
 constexpr int kStagers = 384;              // warps 2..13 stage the activation terms
-constexpr int kTcMaxStages = 8;
+constexpr int kTcMaxStages = 12;
 constexpr int kTcMinStages = 3;
 constexpr int kTcSmem = 227 * 1024;
-constexpr int kDCols = 128;  // tensor-memory columns per accumulator set: 4 k-step chains x 32
-constexpr int kSfCols = 32;  // per ring stage: weight scales 16, activation scales 16
+constexpr int kDCols = 32;   // tensor-memory columns per accumulator
+// A ring stage: the 16 KB nibble box and the 2 KB scale box (both by TMA),
+// then the four 512-byte copy atoms of the weight scales (by the scale
+// warps).
+constexpr int kTcStageBytes = kStageBytes + 2048;
+constexpr int kBoxOff = kPackedStage;
+constexpr int kSfaOff = kStageBytes;
+// Tensor memory: two accumulators (columns 0..63), two weight-scale sets
+// used by alternate units (64..95; copies and MMAs run in issue order, so a
+// set is rewritten only after the MMAs that read it), then the activation-
+// term scales of every staged slot, 16 columns per slot, written once per
+// launch.
+constexpr int kSfaCol = 64;
+constexpr int kSfbCol = 96;
+constexpr int kTcMaxSlots = (512 - kSfbCol) / 16;
+static_assert(kTcStageBytes % 1024 == 0, "stages stay 1 KiB aligned");
 
 struct TcCtrl {
   uint64_t full[kTcMaxStages];
@@ -90,13 +104,11 @@ __host__ __device__ __forceinline__ int tc_b_bytes(int slots, int n) {
 }
 __host__ __device__ __forceinline__ int tc_stages(int slots, int n) {
   const int room = kTcSmem - 1024 - kTcCtrlBytes - tc_b_bytes(slots, n);
-  const int s = room / kStageBytes;
+  const int s = room / kTcStageBytes;
   return s > kTcMaxStages ? kTcMaxStages : s;
 }
-__host__ __device__ __forceinline__ uint32_t tc_tmem_cols(int stages) {
-  return 2 * kDCols + stages * kSfCols <= 256 ? 256u : 512u;
-}
-static_assert(2 * kDCols + kTcMaxStages * kSfCols <= 512, "tensor memory holds 512 columns");
+constexpr uint32_t kTmemCols = 512;
+static_assert(kSfbCol + 16 * kTcMaxSlots <= int(kTmemCols), "tensor-memory budget");
 
 __device__ __forceinline__ void bar_named(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -223,13 +235,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int slots = x_slots(L, units);
 
   uint8_t *ring = base;
-  uint8_t *btile = base + S * kStageBytes;                  // [slots][N rows][128 B]
+  uint8_t *btile = base + S * kTcStageBytes;                // [slots][N rows][128 B]
   uint8_t *bscale = btile + slots * N * 128;                // [slots][4 k-steps][N] words
   TcCtrl &ct = *reinterpret_cast<TcCtrl *>(bscale + slots * 4 * N * 4);
   volatile int *aborted = &ct.aborted;
   p.tm_w = &tm_w;
   p.tm_s = &tm_s;
-  const uint32_t cols = tc_tmem_cols(S);
+  const uint32_t cols = kTmemCols;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -266,10 +278,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (*aborted) break;
         const int64_t rb = u / units;
         const int uk = int(u - rb * units);
-        uint8_t *stage = ring + st * kStageBytes;
+        uint8_t *stage = ring + st * kTcStageBytes;
         mbar_expect_tx(&ct.full[st], kStageBytes);
         tma_load_2d(stage, p.tm_w, uk * kUnitCols, int(rb * kRB), &ct.full[st]);
-        tma_load_2d(stage + kPackedStage, p.tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[st]);
+        tma_load_2d(stage + kBoxOff, p.tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[st]);
       }
       // no copy may still be landing when the CTA exits
       int never = 0;
@@ -279,53 +291,60 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issue
     bar_named(2, kStagers + 32);  // activation terms staged
-    if (lane == 0) {
-      tcx::fence_after_sync();
-      const uint32_t idesc = tcx::idesc_nvf4(N);
-      const uint32_t ring_a = tcx::smem_addr(ring), b_a = tcx::smem_addr(btile);
-      RingPos pos;
-      int uses[2] = {0, 0};
-      int buf = 0;
-      bool ok = !*aborted;
-      int64_t u = u_begin;
-      while (u < u_end && ok) {
-        const int64_t rb = u / units;
-        const int uk0 = int(u - rb * units);
-        const int uk1 = int(uk0 + (u_end - u) < units ? uk0 + (u_end - u) : units);
-        if (uses[buf] > 0 && !wait_or_abort(&ct.accempty[buf], unsigned(uses[buf] - 1) & 1u, aborted, r.status)) {
-          ok = false;
-          break;
-        }
-        int slot = all_units ? uk0 : (uk0 >= uk_begin ? uk0 - uk_begin : uk0 + units - uk_begin);
-        for (int uk = uk0; uk < uk1; ++uk, ++slot, pos.advance(S)) {
-          const int st = pos.st;
-          if (!wait_or_abort(&ct.full[st], pos.phase, aborted, r.status) ||
-              !wait_or_abort(&ct.sfready[st], pos.phase, aborted, r.status)) {
-            ok = false;
-            break;
-          }
-          tcx::fence_after_sync();
-          const uint32_t sf = tmem + 2 * kDCols + st * kSfCols;
-          // k-step j of every unit accumulates into chain j: four
-          // independent accumulators keep the tensor core's pipeline full
+    // The whole warp runs the loop (waits included) and stays converged;
+    // one lane issues the copies, MMAs and commits.
+    tcx::fence_after_sync();
+    const bool leader = lane == 0;
+    const uint32_t idesc = tcx::idesc_nvf4(N);
+    const uint32_t ring_a = tcx::smem_addr(ring), b_a = tcx::smem_addr(btile);
+    RingPos pos;
+    int uses[2] = {0, 0};
+    int buf = 0;
+    bool ok = !*aborted;
+    int64_t u = u_begin;
+    while (u < u_end && ok) {
+      const int64_t rb = u / units;
+      const int uk0 = int(u - rb * units);
+      const int uk1 = int(uk0 + (u_end - u) < units ? uk0 + (u_end - u) : units);
+      if (uses[buf] > 0)
+        ok = __all_sync(0xFFFFFFFFu, wait_or_abort(&ct.accempty[buf], unsigned(uses[buf] - 1) & 1u,
+                                                    aborted, r.status));
+      if (!ok) break;
+      int slot = all_units ? uk0 : (uk0 >= uk_begin ? uk0 - uk_begin : uk0 + units - uk_begin);
+      for (int uk = uk0; uk < uk1; ++uk, ++slot, pos.advance(S)) {
+        const int st = pos.st;
+        ok = __all_sync(0xFFFFFFFFu, wait_or_abort(&ct.full[st], pos.phase, aborted, r.status) &&
+                                         wait_or_abort(&ct.sfready[st], pos.phase, aborted, r.status));
+        if (!ok) break;
+        tcx::fence_after_sync();
+        const uint32_t stage_a = ring_a + st * kTcStageBytes;
+        const uint32_t sfa = tmem + kSfaCol + uint32_t(pos.count & 1) * 16;
+        const uint32_t sfb = tmem + kSfbCol + slot * 16;
+        if (leader) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) tcx::cp_atom(sfa + 4 * j, tcx::desc_atom(stage_a + kSfaOff + 512 * j));
 #pragma unroll
           for (int j = 0; j < 4; ++j)
-            tcx::mma_nvf4(tmem + buf * kDCols + 32 * j,
-                          tcx::desc_k_sw128(ring_a + st * kStageBytes + 32 * j),
-                          tcx::desc_k_sw128(b_a + slot * N * 128 + 32 * j), idesc, sf + 4 * j,
-                          sf + 16 + 4 * j, uk > uk0);
+            tcx::mma_nvf4(tmem + buf * kDCols, tcx::desc_k_sw128(stage_a + 32 * j),
+                          tcx::desc_k_sw128(b_a + slot * N * 128 + 32 * j), idesc, sfa + 4 * j,
+                          sfb + 4 * j, uk > uk0 || j > 0);
           tcx::commit_to(&ct.empty[st]);
         }
-        if (!ok) break;
-        tcx::commit_to(&ct.accfull[buf]);
-        ++uses[buf];
-        buf ^= 1;
-        u += uk1 - uk0;
+        __syncwarp();
       }
+      if (!ok) break;
+      if (leader) tcx::commit_to(&ct.accfull[buf]);
+      __syncwarp();
+      ++uses[buf];
+      buf ^= 1;
+      u += uk1 - uk0;
+    }
+    if (leader) {
       tcx::commit_to(&ct.mma_done);
       int never = 0;
       mbar_wait(&ct.mma_done, 0, &never);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ warps 2..13
     const int tid = threadIdx.x - 64;  // 0..383
@@ -368,6 +387,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
     tcx::fence_async_smem();
+    bar_named(1, kStagers);
+    if (warp < kWarpEpi) {
+      // Activation-term scales of every slot into tensor memory, once: B
+      // row n's word of k-step j at column kSfbCol + 16 slot + 4 j, lane
+      // n % 32 of every quarter (one warp per quarter; rows n < N <= 32).
+      const uint32_t lb = tmem + (uint32_t((warp & 3) * 32) << 16) + kSfbCol;
+      const uint32_t *bw = reinterpret_cast<const uint32_t *>(bscale);
+      for (int sl = 0; sl < slots; ++sl) {
+        uint32_t v[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[4 * j] = lane < N ? bw[(sl * 4 + j) * N + lane] : 0u;
+          v[4 * j + 1] = 0u;
+          v[4 * j + 2] = 0u;
+          v[4 * j + 3] = 0u;
+        }
+        tcx::st_x16(lb + 16 * sl, v);
+      }
+      tcx::wait_st();
+    }
+    tcx::fence_before_sync();
     bar_named(2, kStagers + 32);  // with the MMA warp
     const float gd = __ldg(p.g_dec);
     const int q = warp & 3;                       // tensor-memory lane quarter
@@ -375,41 +415,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (warp < kWarpEpi) {
       // ---------------------------------------------------------- scales
+      // Thread t of the four scale warps owns weight row t of the unit: it
+      // gathers the row's 16 scale bytes from the tile layout and writes
+      // them as its words of the four copy atoms (one per 64-column
+      // k-step).  No barrier spans the warps.
+      const int t = threadIdx.x - 64;  // 0..127
+      const int rt = t >> 4, h = (t >> 3) & 1, g = t & 7;
       RingPos pos;
       for (int64_t u = u_begin; u < u_end && !*aborted; ++u, pos.advance(S)) {
         const int st = pos.st;
         const int64_t rb = u / units;
         const int uk = int(u - rb * units);
-        const int slot = all_units ? uk : (uk >= uk_begin ? uk - uk_begin : uk + units - uk_begin);
         if (!wait_or_abort(&ct.full[st], pos.phase, aborted, r.status)) break;
-        tcx::fence_after_sync();  // the MMAs that read this stage's scale columns are done
-        const uint8_t *sbox = ring + st * kStageBytes + kPackedStage;
-        uint32_t va[16], vb[16];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int row = 32 * c + lane;
-          const int rt = row >> 4, h = (row >> 3) & 1, g = row & 7;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int off = rt * 256 + (j >> 1) * 128 + (4 * g + 2 * (j & 1)) * 4 + 2 * h;
-            const uint32_t lo = *reinterpret_cast<const uint16_t *>(sbox + off);
-            const uint32_t hi = *reinterpret_cast<const uint16_t *>(sbox + off + 4);
-            va[4 * j + c] = lo | (hi << 16);
-          }
-        }
-        const uint32_t *bw = reinterpret_cast<const uint32_t *>(bscale) + slot * 4 * N;
+        uint8_t *stage = ring + st * kTcStageBytes;
+        uint32_t wa[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          vb[4 * j] = lane < N ? bw[j * N + lane] : 0u;
-          vb[4 * j + 1] = 0u;
-          vb[4 * j + 2] = 0u;
-          vb[4 * j + 3] = 0u;
+          const int off = kBoxOff + rt * 256 + (j >> 1) * 128 + (4 * g + 2 * (j & 1)) * 4 + 2 * h;
+          const uint32_t lo = *reinterpret_cast<const uint16_t *>(stage + off);
+          const uint32_t hi = *reinterpret_cast<const uint16_t *>(stage + off + 4);
+          wa[j] = lo | (hi << 16);
         }
-        const uint32_t sf = lane_base + 2 * kDCols + st * kSfCols;
-        tcx::st_x16(sf, va);
-        tcx::st_x16(sf + 16, vb);
-        tcx::wait_st();
-        tcx::fence_before_sync();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint32_t *>(stage + kSfaOff + 512 * j + (t & 31) * 16 + (t >> 5) * 4) = wa[j];
+        tcx::fence_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ct.sfready[st]);
       }
@@ -425,21 +455,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int uk1 = int(uk0 + (u_end - u) < units ? uk0 + (u_end - u) : units);
         const bool ok = wait_or_abort(&ct.accfull[buf], unsigned(uses[buf]) & 1u, aborted, r.status);
         tcx::fence_after_sync();
-        // the four chains, added in a fixed order
         float d[32];
+        {
+          uint32_t h0[16], h1[16];
+          tcx::ld_x16(lane_base + buf * kDCols, h0);
+          if (N > 16) tcx::ld_x16(lane_base + buf * kDCols + 16, h1);
+          tcx::wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) d[i] = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            if (half == 1 && N <= 16) break;
-            uint32_t h[16];
-            tcx::ld_x16(lane_base + buf * kDCols + 32 * j + 16 * half, h);
-            tcx::wait_ld();
-#pragma unroll
-            for (int i = 0; i < 16; ++i) d[16 * half + i] = __fadd_rn(d[16 * half + i], __uint_as_float(h[i]));
+          for (int i = 0; i < 16; ++i) {
+            d[i] = __uint_as_float(h0[i]);
+            d[16 + i] = N > 16 ? __uint_as_float(h1[i]) : 0.0f;
           }
+        }
         tcx::fence_before_sync();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ct.accempty[buf]);
@@ -552,7 +579,7 @@ bool tc_eligible(int n, int k, int m, const DeviceInfo &dev) {
   const GemvPlan p = plan_gemv_tc(n, k, dev);
   const int64_t longest = ceil_div(p.total, p.grid);
   const int slots = x_slots(longest, int(p.units));
-  return slots <= 64 && tc_stages(slots, 32) >= kTcMinStages;
+  return slots <= kTcMaxSlots && tc_stages(slots, 32) >= kTcMinStages;
 }
 
 size_t gemv_tc_workspace_bytes(int n, int k, const DeviceInfo &dev) {

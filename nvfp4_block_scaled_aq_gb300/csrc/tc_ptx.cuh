@@ -17,6 +17,12 @@
 //    same holds for the B operand with its column index n in place of r.
 //  * The accumulator of an M = 128 MMA holds row r in TMEM lane r and output
 //    column n in column d0 + n (fp32).
+//  * tcgen05.cp 32x128b.warpx4 copies a 512-byte shared-memory atom (32 rows
+//    of 16 B, no swizzle, 8-row core matrices 128 B apart) into 4 columns of
+//    every 32-lane quarter: lane 32q + i, column c0 + c receives atom bytes
+//    16i + 4c .. 16i + 4c + 3.  So an MMA's 128 x 4 scales, row r's four
+//    bytes at atom offset (r % 32) * 16 + (r / 32) * 4, land exactly in the
+//    layout above.
 #pragma once
 
 #include <cstdint>
@@ -69,6 +75,20 @@ __device__ __forceinline__ void fence_after_sync() {
 // Generic-proxy shared-memory writes become visible to the tensor core.
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Shared-memory descriptor of a copy atom: no swizzle, 8-row core matrices
+// of 16-byte rows, 128 B apart (leading and stride offsets both 128 B).
+__device__ __forceinline__ uint64_t desc_atom(uint32_t addr) {
+  return uint64_t((addr & 0x3FFFFu) >> 4) | (uint64_t(128 >> 4) << 16) |
+         (uint64_t(128 >> 4) << 32) | (uint64_t(1) << 46);
+}
+
+// Shared-memory atom -> 4 tensor-memory columns (replicated over the four
+// lane quarters); issued by one thread, ordered with its MMAs.
+__device__ __forceinline__ void cp_atom(uint32_t taddr, uint64_t src_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc)
+               : "memory");
 }
 
 // D (+)= A * B with block scales; issued by one thread.
