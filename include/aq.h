@@ -95,6 +95,8 @@ typedef struct {
 /* Shape limits: 1 <= n <= 2^24, 32 <= k <= 2^20, k % 32 == 0,
  * 0 <= r <= 64, 1 <= m <= AQ_MAX_M for the GEMV path. */
 #define AQ_MAX_M 16
+/* Tokens the block-scaled MMA path (AQ_PATH_MMA) serves per call. */
+#define AQ_MAX_M_MMA 64
 
 /* Bytes of the packed nibbles and of the scale layout of an [n, k] weight.
  * For n % 16 == 0 and k % 128 == 0 the two add up to 0.5625 * n * k.
@@ -155,7 +157,7 @@ AQ_API aq_status aq_reconstruct_quantize_nvfp4(const uint16_t *W0, const float *
  * register-decode one); the explicit choices exist for testing and
  * measurement. */
 typedef enum {
-  AQ_PATH_AUTO = 0,           /* choose by m                                 */
+  AQ_PATH_AUTO = 0,           /* GEMV for m <= AQ_MAX_M, MMA above           */
   AQ_PATH_GEMV = 1,           /* bf16 activations, kernel chosen by m        */
   AQ_PATH_MMA = 2,            /* activations quantised to NVFP4, tcgen05 MMA */
   AQ_PATH_GEMV_REGDECODE = 3, /* bf16 activations, register-decode kernel    */
@@ -164,11 +166,12 @@ typedef enum {
 } aq_path;
 
 /* Workspace of aq_gemv_nvfp4 / aq_decode_step_weights for a weight of
- * shape [n, k] and m tokens: bytes, device memory, 256-byte aligned.  It
- * must be ZERO-FILLED once after allocation; every call leaves it in the
- * state it needs next, so one zeroed workspace serves any sequence of
- * calls on one stream.  Calls that may run concurrently need separate
- * workspaces. */
+ * shape [n, k] and m tokens (1 <= m <= AQ_MAX_M_MMA): bytes, device memory,
+ * 256-byte aligned, enough for every path that serves m tokens (for the
+ * MMA path it also holds the quantised activations).  It must be
+ * ZERO-FILLED once after allocation; every call leaves it in the state it
+ * needs next, so one zeroed workspace serves any sequence of calls on one
+ * stream.  Calls that may run concurrently need separate workspaces. */
 AQ_API size_t aq_gemv_workspace_bytes(int32_t n, int32_t k, int32_t m);
 
 /* y[t, i] = bf16( sum_k x[t, k] * w_hat[i, k] ), w_hat = e2m1(q)*sd*g_dec,
@@ -183,6 +186,28 @@ AQ_API size_t aq_gemv_workspace_bytes(int32_t n, int32_t k, int32_t m);
 AQ_API aq_status aq_gemv_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m,
                         uint16_t *y, aq_path path, void *workspace,
                         size_t workspace_bytes, aq_stream_t stream);
+
+/* The block-scaled MMA path (AQ_PATH_MMA, and AQ_PATH_AUTO for m > AQ_MAX_M;
+ * 1 <= m <= AQ_MAX_M_MMA).  AttnQuant docs, "Throughput", per-kernel
+ * profile: the serving stack's NVFP4 projections are block-scaled fp4 GEMMs
+ * that quantise the activations.  Each token row of x is first quantised on
+ * its own exactly as aq_quantize_act_nvfp4 does (into the workspace); then
+ *   y[t, i] = bf16( g_dec_w * g_dec_x[t] * sum_j sd_w[i, j] * sd_x[t, j]
+ *                   * sum_{k in block j} e2m1(q_w[i, k]) * e2m1(q_x[t, k]) )
+ * with fp32 accumulation on the tcgen05 tensor cores.  Outputs are within
+ * the GEMV tolerance of the exact product of the two dequantised operands,
+ * independent of timing, and each token's output does not depend on m.
+ *
+ * Per-row NVFP4 quantisation of activations (x [m, k] bf16 row-major,
+ * 16-byte aligned): for each row its own amax, g_enc = 2688/amax,
+ * g_dec[t] = amax/2688, and the block steps of aq_quantize_nvfp4.  packed
+ * [m, k/2] (16-byte aligned), scales [m, k/16] E4M3 in canonical row-major
+ * order (no tile layout), g_dec [m] fp32.  A row whose amax is non-finite or
+ * too small is zero-filled, gets a NaN g_dec, and the next
+ * aq_poll_device_status() returns AQ_ERR_RANGE.  1 <= m <= 2^20. */
+AQ_API aq_status aq_quantize_act_nvfp4(const uint16_t *x, int32_t m, int32_t k,
+                                       uint8_t *packed, uint8_t *scales, float *g_dec,
+                                       aq_stream_t stream);
 
 /* aq_gemv_nvfp4 without a workspace argument, for callers that cannot
  * allocate device memory: a plugin inside a host program that owns every

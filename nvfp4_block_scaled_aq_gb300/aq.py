@@ -32,6 +32,7 @@ STEP_PDL = 1
 STEP_REGDECODE = 2
 STEP_TCGEN05 = 4
 MAX_M = 16
+MAX_M_MMA = 64
 NOALLOC_MAX_SCRATCH = 8 << 20  # AQ_GEMV_NOALLOC_MAX_SCRATCH
 
 
@@ -85,6 +86,7 @@ def _declare(L):
         "aq_gemv_workspace_bytes": ([_i32, _i32, _i32], _sz),
         "aq_gemv_nvfp4": ([W, _p, _i32, _p, C.c_int, _p, _sz, _p], C.c_int),
         "aq_gemv_nvfp4_noalloc": ([W, _p, _i32, _p, C.c_int, _p], C.c_int),
+        "aq_quantize_act_nvfp4": ([_p, _i32, _i32, _p, _p, _p, _p], C.c_int),
         "aq_decode_step_weights": ([W, _i32, C.POINTER(_p), C.POINTER(_p), _i32,
                                     C.c_uint32, _p, _sz, _p], C.c_int),
         "aq_scales_to_canonical": ([W, _p, _p], C.c_int),
@@ -203,6 +205,13 @@ def gemv(w: Nvfp4Weight, x, y, workspace, path=PATH_AUTO, stream=None):
     check(lib().aq_gemv_nvfp4(C.byref(wc), _ptr(x), m, _ptr(y), path, _ptr(workspace),
                               workspace.numel() * workspace.element_size(),
                               _stream(stream)))
+
+
+def quantize_act(x, packed, scales, g_dec, stream=None):
+    """Per-row NVFP4 quantisation of activations x [m, k] (canonical scales)."""
+    m, k = x.shape
+    check(lib().aq_quantize_act_nvfp4(_ptr(x), m, k, _ptr(packed), _ptr(scales), _ptr(g_dec),
+                                      _stream(stream)))
 
 
 def gemv_noalloc(w: Nvfp4Weight, x, y, path=PATH_AUTO, stream=None):

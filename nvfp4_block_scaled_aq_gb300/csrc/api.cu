@@ -213,11 +213,40 @@ aq_status aq_reconstruct_quantize_nvfp4(const uint16_t *W0, const float *s, cons
   return quantize_common(W0, s, U, V, n, k, r, true, out, workspace, workspace_bytes, stream);
 }
 
+aq_status aq_quantize_act_nvfp4(const uint16_t *x, int32_t m, int32_t k, uint8_t *packed,
+                                uint8_t *scales, float *g_dec, aq_stream_t stream) {
+  const char *what = "aq_quantize_act_nvfp4";
+  if (m < 1 || m > (1 << 20))
+    return set_error(AQ_ERR_SHAPE, "%s: m = %d outside [1, 2^20]", what, m);
+  aq_status s = check_nk(1, k);
+  if (s != AQ_OK) return s;
+  if (!x || !packed || !scales || !g_dec)
+    return set_error(AQ_ERR_INVALID_ARG, "%s: pointers must not be NULL", what);
+  if (!aligned(x, 16) || !aligned(packed, 16) || !aligned(g_dec, 4))
+    return set_error(AQ_ERR_ALIGNMENT, "%s: x and packed must be 16-byte aligned, g_dec 4-byte",
+                     what);
+  const DeviceInfo *dev = device_info();
+  if (!dev) return AQ_ERR_UNSUPPORTED;
+  return launched(launch_act_quant(x, m, k, packed, scales, k / 16, g_dec, *dev,
+                                   reinterpret_cast<cudaStream_t>(stream)),
+                  what);
+}
+
+// Enough for every path that serves m tokens.
+static size_t workspace_for(int32_t n, int32_t k, int32_t m, const DeviceInfo &dev) {
+  size_t b = gemv_workspace_bytes(n, k, dev);
+  if (m <= AQ_MAX_M_MMA) {
+    const size_t mb = mma_workspace(n, k, m, dev).bytes;
+    if (mb > b) b = mb;
+  }
+  return b;
+}
+
 size_t aq_gemv_workspace_bytes(int32_t n, int32_t k, int32_t m) {
-  if (check_nk(n, k) != AQ_OK || m < 1 || m > AQ_MAX_M) return 0;
+  if (check_nk(n, k) != AQ_OK || m < 1 || m > AQ_MAX_M_MMA) return 0;
   const DeviceInfo *dev = device_info();
   if (!dev) return 0;
-  return gemv_workspace_bytes(n, k, *dev);
+  return workspace_for(n, k, m, *dev);
 }
 
 // Host-only checks of one GEMV call (no device query).
@@ -225,13 +254,12 @@ aq_status gemv_args(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m,
                            const uint16_t *y, aq_path path, const char *what) {
   aq_status s = check_weight(w, what);
   if (s != AQ_OK) return s;
-  if (m < 1 || m > AQ_MAX_M)
-    return set_error(AQ_ERR_SHAPE, "%s: m = %d outside [1, %d]", what, m, AQ_MAX_M);
-  if (path == AQ_PATH_MMA)
-    return set_error(AQ_ERR_UNSUPPORTED, "%s: the MMA path is not built in this version", what);
-  if (path != AQ_PATH_AUTO && path != AQ_PATH_GEMV && path != AQ_PATH_GEMV_REGDECODE &&
-      path != AQ_PATH_GEMV_TCGEN05)
+  if (path != AQ_PATH_AUTO && path != AQ_PATH_GEMV && path != AQ_PATH_MMA &&
+      path != AQ_PATH_GEMV_REGDECODE && path != AQ_PATH_GEMV_TCGEN05)
     return set_error(AQ_ERR_INVALID_ARG, "%s: unknown path %d", what, int(path));
+  const int32_t max_m = (path == AQ_PATH_MMA || path == AQ_PATH_AUTO) ? AQ_MAX_M_MMA : AQ_MAX_M;
+  if (m < 1 || m > max_m)
+    return set_error(AQ_ERR_SHAPE, "%s: m = %d outside [1, %d] for this path", what, m, max_m);
   if (!x || !y) return set_error(AQ_ERR_INVALID_ARG, "%s: x and y must not be NULL", what);
   if (!aligned(x, 16) || !aligned(y, 16))
     return set_error(AQ_ERR_ALIGNMENT, "%s: x and y must be 16-byte aligned", what);
@@ -246,9 +274,16 @@ aq_status aq_gemv_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m, 
   if (s != AQ_OK) return s;
   const DeviceInfo *dev = device_info();
   if (!dev) return AQ_ERR_UNSUPPORTED;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (path == AQ_PATH_MMA || (path == AQ_PATH_AUTO && m > AQ_MAX_M)) {
+    if (!mma_eligible(w->n, w->k, m, *dev))
+      return set_error(AQ_ERR_UNSUPPORTED, "%s: the MMA path does not serve m = %d", what, m);
+    if ((s = check_ws(workspace, workspace_bytes, mma_workspace(w->n, w->k, m, *dev).bytes, what)) != AQ_OK)
+      return s;
+    return launched(launch_mma(*w, x, m, y, workspace, false, *dev, st), what);
+  }
   if ((s = check_ws(workspace, workspace_bytes, gemv_workspace_bytes(w->n, w->k, *dev), what)) != AQ_OK)
     return s;
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   if (path == AQ_PATH_GEMV_REGDECODE)
     return launched(launch_gemv_regdecode(*w, x, m, y, workspace, false, *dev, st), what);
   if (path == AQ_PATH_GEMV_TCGEN05) {

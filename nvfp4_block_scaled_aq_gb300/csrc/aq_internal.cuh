@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <cuda.h>
+
 #include "../../include/aq.h"
 
 namespace aq {
@@ -180,6 +182,11 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
                             const uint16_t *V, int r, bool fused, int n, int k,
                             const aq_nvfp4_weight &out, void *ws, const DeviceInfo &dev,
                             cudaStream_t st);
+// Per-row NVFP4 quantisation of activations (quantize.cu); scales row-major
+// with a pitch of scale_pitch bytes.
+cudaError_t launch_act_quant(const uint16_t *x, int m, int k, uint8_t *packed, uint8_t *scales,
+                             int scale_pitch, float *g_dec, const DeviceInfo &dev,
+                             cudaStream_t st);
 cudaError_t launch_scales_to_canonical(const aq_nvfp4_weight &w, uint8_t *canon,
                                        cudaStream_t st);
 
@@ -202,6 +209,22 @@ bool tc_eligible(int n, int k, int m, const DeviceInfo &dev);
 size_t gemv_tc_workspace_bytes(int n, int k, const DeviceInfo &dev);
 cudaError_t launch_gemv_tc(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
                            void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st);
+// The block-scaled MMA path (mma_gemm.cu): workspace layout for m tokens,
+// eligibility, and the launch of activation quantisation + MMA kernel.
+struct MmaWorkspace {
+  int slots;                 // partial-sum token slots per row
+  int scale_pitch;           // bytes per row of the activation scales
+  size_t partial_off, xq_off, xs_off, xg_off, bytes;
+};
+MmaWorkspace mma_workspace(int n, int k, int m, const DeviceInfo &dev);
+bool mma_eligible(int n, int k, int m, const DeviceInfo &dev);
+cudaError_t launch_mma(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y, void *ws,
+                       bool pdl, const DeviceInfo &dev, cudaStream_t st);
+// Tensor maps of quantised activations: nibbles [m, k/2] in boxes of
+// 128 B x n_box rows (128-byte swizzle) and scales [m rows, pitch bytes] in
+// boxes of 16 B x n_box rows (gemv.cu).
+bool encode_act_maps(const uint8_t *xq, const uint8_t *xs, int m, int k, int scale_pitch,
+                     int n_box, CUtensorMap *tm_x, CUtensorMap *tm_xs);
 // Register-decode kernel only (gemv.cu).
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,

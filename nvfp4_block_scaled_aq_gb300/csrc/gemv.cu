@@ -197,6 +197,20 @@ bool encode_maps(const aq_nvfp4_weight &w, CUtensorMap *tm_w, CUtensorMap *tm_s)
 
 }  // namespace core
 
+bool encode_act_maps(const uint8_t *xq, const uint8_t *xs, int m, int k, int scale_pitch,
+                     int n_box, CUtensorMap *tm_x, CUtensorMap *tm_xs) {
+  if (!encoder()) return false;
+  // k/16 scale columns of a row; the pitch pads the row to 16 bytes
+  const cuuint64_t dims[2] = {cuuint64_t(k / 16), cuuint64_t(m)};
+  const cuuint64_t strides[1] = {cuuint64_t(scale_pitch)};
+  const cuuint32_t box[2] = {16, cuuint32_t(n_box)};
+  const cuuint32_t estr[2] = {1, 1};
+  return cached_map(tm_x, xq, uint64_t(k) / 2, uint64_t(m), kUnitCols, uint32_t(n_box), true) &&
+         g_encode(tm_xs, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(xs), dims,
+                  strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev) {
   GemvPlan p;
   p.row_blocks = ceil_div(n, kRB);

@@ -63,8 +63,9 @@ aq_status aq_gemv_nvfp4_noalloc(const aq_nvfp4_weight *w, const uint16_t *x, int
   const char *what = "aq_gemv_nvfp4_noalloc";
   aq_status s = gemv_args(w, x, m, y, path, what);
   if (s != AQ_OK) return s;
-  if (path == AQ_PATH_GEMV_TCGEN05)
-    return set_error(AQ_ERR_UNSUPPORTED, "%s: runs the register-decode kernel only", what);
+  if (path == AQ_PATH_GEMV_TCGEN05 || path == AQ_PATH_MMA || m > AQ_MAX_M)
+    return set_error(AQ_ERR_UNSUPPORTED, "%s: runs the register-decode kernel only (m <= %d)",
+                     what, AQ_MAX_M);
   const DeviceInfo *dev = device_info();
   if (!dev) return AQ_ERR_UNSUPPORTED;
   const size_t need = gemv_workspace_bytes(w->n, w->k, *dev);

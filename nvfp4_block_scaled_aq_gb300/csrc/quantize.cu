@@ -265,6 +265,54 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
+// Activations for the block-scaled MMA path (reading R9: each token row
+// quantised on its own, with the per-tensor steps applied per row): one CTA
+// per row.  packed [m, k/2], scales [m, k/16] row-major with a row pitch of
+// scale_pitch bytes (k/16 for the canonical layout), g_dec [m].  A row whose amax is out of range is zero-filled, gets a NaN
+// g_dec and raises AQ_ERR_RANGE.
+__global__ void __launch_bounds__(kThreads)
+    act_quant_kernel(const uint16_t *__restrict__ x, int k, uint8_t *__restrict__ packed,
+                     uint8_t *__restrict__ scales, int scale_pitch, float *__restrict__ g_dec,
+                     unsigned *status) {
+  __shared__ uint32_t amax_s;
+  const int64_t row = blockIdx.x;
+  const uint16_t *xr = x + row * k;
+  uint32_t m2 = 0;
+  for (int i = threadIdx.x * 8; i < k; i += kThreads * 8) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + i));
+    m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
+    m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
+  }
+  const uint32_t m = block_max_u32(max(m2 & 0xFFFFu, m2 >> 16));
+  if (threadIdx.x == 0) amax_s = m;
+  __syncthreads();
+  float g_enc = 1.0f, gd = 1.0f;
+  const bool ok = global_scales(amax_s, g_enc, gd);
+  if (threadIdx.x == 0) {
+    g_dec[row] = ok ? gd : __int_as_float(0x7FC00000);
+    if (!ok) raise_status(status, kDevRange);
+  }
+  for (int b = threadIdx.x; b < k / kBlock; b += kThreads) {
+    float w[16];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + b * kBlock) + q);
+      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        w[8 * q + 2 * i] = bf16_lo(vv[i]);
+        w[8 * q + 2 * i + 1] = bf16_hi(vv[i]);
+      }
+    }
+    uint32_t lo = 0, hi = 0, sf = 0;
+    if (ok) sf = quantize_block(w, g_enc, lo, hi);
+    *reinterpret_cast<uint2 *>(packed + row * (k / 2) + b * 8) = make_uint2(lo, hi);
+    scales[row * scale_pitch + b] = uint8_t(sf);
+  }
+}
+
 __global__ void scales_to_canonical_kernel(const uint8_t *__restrict__ scales, int n,
                                            int k, uint8_t *__restrict__ canon) {
   const int64_t nblk = k / kBlock;
@@ -333,6 +381,13 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
     quantize_pass<4, true>(W, s, U, V, r, n, k, out, amax, dev, st);
   else
     quantize_pass<-1, true>(W, s, U, V, r, n, k, out, amax, dev, st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_act_quant(const uint16_t *x, int m, int k, uint8_t *packed, uint8_t *scales,
+                             int scale_pitch, float *g_dec, const DeviceInfo &dev,
+                             cudaStream_t st) {
+  act_quant_kernel<<<m, kThreads, 0, st>>>(x, k, packed, scales, scale_pitch, g_dec, dev.status);
   return cudaGetLastError();
 }
 

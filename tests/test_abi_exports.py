@@ -76,8 +76,20 @@ def test_host_validation_without_a_device(aq):
     ok_w = aq.Nvfp4WeightC(16, 64, 256, 256, 256)
     assert L.aq_gemv_nvfp4(C.byref(ok_w), C.c_void_p(16), 0, C.c_void_p(16), 0,
                            None, 0, None) == aq.ERR_SHAPE
-    assert L.aq_gemv_nvfp4(C.byref(ok_w), C.c_void_p(16), 17, C.c_void_p(16), 0,
+    # the GEMV paths take up to AQ_MAX_M tokens, the MMA path (and AUTO) up to
+    # AQ_MAX_M_MMA
+    assert L.aq_gemv_nvfp4(C.byref(ok_w), C.c_void_p(16), 17, C.c_void_p(16), aq.PATH_GEMV,
                            None, 0, None) == aq.ERR_SHAPE
+    assert L.aq_gemv_nvfp4(C.byref(ok_w), C.c_void_p(16), 65, C.c_void_p(16), aq.PATH_AUTO,
+                           None, 0, None) == aq.ERR_SHAPE
+    assert L.aq_gemv_nvfp4(C.byref(ok_w), C.c_void_p(16), 65, C.c_void_p(16), aq.PATH_MMA,
+                           None, 0, None) == aq.ERR_SHAPE
+    assert L.aq_quantize_act_nvfp4(C.c_void_p(16), 0, 64, C.c_void_p(16), C.c_void_p(16),
+                                   C.c_void_p(16), None) == aq.ERR_SHAPE
+    assert L.aq_quantize_act_nvfp4(C.c_void_p(16), 2, 48, C.c_void_p(16), C.c_void_p(16),
+                                   C.c_void_p(16), None) == aq.ERR_SHAPE
+    assert L.aq_quantize_act_nvfp4(C.c_void_p(8), 2, 64, C.c_void_p(16), C.c_void_p(16),
+                                   C.c_void_p(16), None) == aq.ERR_ALIGNMENT
     assert L.aq_gemv_nvfp4(C.byref(ok_w), C.c_void_p(16), 1, C.c_void_p(16), 7,
                            None, 0, None) == aq.ERR_INVALID_ARG
     assert L.aq_reconstruct(None, None, None, None, 16, 64, 0, None, None) == \
