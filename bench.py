@@ -58,6 +58,12 @@ def parse():
     p.add_argument("--workload", choices=("31b", "1b"), default="31b")
     p.add_argument("--layers", type=int, default=0,
                    help="stream only the first L layers (0: all of the workload's layers)")
+    p.add_argument("--batch-sweep", action="store_true",
+                   help="time the ~31B-shaped fused gate+up and down weights at M in "
+                        "{1, 2, 4, 8, 16, 32, 64} on every path instead of the step")
+    p.add_argument("--sweep-m", type=str, default="",
+                   help="comma-separated subset of the sweep's M values (profiling)")
+    p.add_argument("--sweep-proj", choices=("both", "gate_up", "down"), default="both")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the eager / no-PDL / end-to-end / CPU-baseline legs")
     return p.parse_args()
@@ -472,6 +478,101 @@ def run_aq(a, dist):
         print(json.dumps(out), flush=True)
 
 
+# ------------------------------------------------------------ batch sweep
+
+SWEEP_M = (1, 2, 4, 8, 16, 32, 64)
+
+
+def run_sweep(a, dist):
+    """GEMV kernels vs the block-scaled MMA path on the ~31B-shaped fused
+    gate+up [43008, 5376] and down [5376, 21504] weights.  Each timing is a
+    CUDA graph of back-to-back calls that rotate over enough weight copies
+    to exceed L2, replayed between CUDA events on the launching stream."""
+    import torch
+    from nvfp4_block_scaled_aq_gb300 import aq, inputs
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(dist.local)
+    device = torch.device("cuda", dist.local)
+    stream = torch.cuda.Stream(device)
+    qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+    results = []
+    ms = tuple(int(v) for v in a.sweep_m.split(",")) if a.sweep_m else SWEEP_M
+    projs = {"both": (2, 3), "gate_up": (2,), "down": (3,)}[a.sweep_proj]
+    for proj in projs:
+        n, k = inputs.LAYER_31B[proj]
+        wbytes = n * k // 2 + n * k // 16
+        copies = max(2, -(-3 * 129 * 2 ** 20 // wbytes))  # at least ~3x L2 in rotation
+        weights = []
+        for c in range(copies):
+            W = inputs.weight(n, k, seed=inputs.seed_of(0, c, proj), device=device)
+            w = aq.Nvfp4Weight.empty(n, k, device=device)
+            aq.quantize(W, w, qws)
+            del W
+            weights.append(w)
+        torch.cuda.synchronize()  # everything below runs on `stream`
+        for m in ms:
+            x = inputs.tokens(m, k, seed=inputs.seed_of(1, 0, proj) + m, device=device)
+            y = torch.empty((m, n), dtype=torch.bfloat16, device=device)
+            ws = torch.zeros(aq.gemv_workspace_bytes(n, k, m), dtype=torch.uint8, device=device)
+            torch.cuda.synchronize()  # x, y and ws are ready before `stream` uses them
+            paths = [("mma", aq.PATH_MMA)]
+            if m <= aq.MAX_M:
+                paths.insert(0, ("gemv_regdecode", aq.PATH_GEMV_REGDECODE))
+            if m <= 5:
+                paths.insert(1, ("gemv_tcgen05", aq.PATH_GEMV_TCGEN05))
+            row = {"proj": "gate_up" if proj == 2 else "down", "n": n, "k": k, "m": m}
+            alg = wbytes + 4 + 2 * m * k + 2 * m * n
+            for name, path in paths:
+                calls = 4 * copies
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.stream(stream):
+                    for w in weights:
+                        aq.gemv(w, x, y, ws, path=path, stream=stream)
+                    stream.synchronize()
+                    with torch.cuda.graph(g, stream=stream):
+                        for i in range(calls):
+                            aq.gemv(weights[i % copies], x, y, ws, path=path, stream=stream)
+
+                def run():
+                    with torch.cuda.stream(stream):
+                        g.replay()
+                reps = max(3, a.steps // 20)
+                secs = time_region(run, reps, max(3, a.warmup), stream, dist)
+                us = secs / (reps * calls) * 1e6
+                row[name] = {"us": round(us, 2), "GBps": round(alg / us / 1e3, 1)}
+                del g
+            st = aq.poll_device_status()
+            if st != aq.OK:
+                raise RuntimeError("device status %d in the sweep" % st)
+            results.append(row)
+            torch.cuda.synchronize()  # `stream` is done with x, y and ws before they are freed
+        torch.cuda.synchronize()
+        del weights
+    crossover = {}
+    for pname in ("gate_up", "down"):
+        rows = [r for r in results if r["proj"] == pname]
+        cross = None
+        for r in rows:
+            gemv = [r[kname]["us"] for kname in ("gemv_regdecode", "gemv_tcgen05") if kname in r]
+            if gemv and r["mma"]["us"] < min(gemv):
+                cross = r["m"]
+                break
+        crossover[pname] = cross
+    peak, peak_kind = load_peaks()
+    out = {"metric": "NVFP4 GEMV vs block-scaled MMA, us per call and GB/s by batch",
+           "value": None, "unit": "GB/s", "n_gpus": dist.world,
+           "higher_is_better": True, "data": "synthetic (seeded)",
+           "config": {"workload": "batch sweep on ~31B-shaped fused gate+up [43008, 5376] and "
+                                  "down [5376, 21504]", "m": list(ms),
+                      "l2": "each graph rotates over enough weight copies to exceed L2"},
+           "sweep": results,
+           "crossover_m_mma_faster": crossover,
+           "hbm_peak_gbs": peak, "hbm_peak_source": peak_kind}
+    if dist.rank == 0:
+        print(json.dumps(out), flush=True)
+
+
 # ------------------------------------------------------------ reference arm
 
 def run_reference(a, dist):
@@ -528,6 +629,8 @@ def main():
     try:
         if a.impl == "reference":
             run_reference(a, dist)
+        elif a.batch_sweep:
+            run_sweep(a, dist)
         else:
             run_aq(a, dist)
     finally:

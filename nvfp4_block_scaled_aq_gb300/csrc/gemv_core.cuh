@@ -33,9 +33,10 @@ constexpr int kSmemBudget = 113 * 1024;         // per CTA, so two fit on an SM
 constexpr int kXChunkBudget = 16;               // m * units staged at once (chunked mode)
 constexpr int kTileHalves = 128;                // f16 per staged 128-column tile
 constexpr unsigned kSpinLimit = 1u << 22;
-// Ticket region of fixed size at the start of a GEMV workspace (one 32-bit
-// ticket per row block of the largest legal n), then the fp32 partials.
-constexpr size_t kTicketBytes = size_t(((1 << 24) + kRB - 1) / kRB) * 4;
+// Ticket region of fixed size at the start of a GEMV workspace (four 32-bit
+// tickets per row block of the largest legal n: one per 32-row quarter for
+// the kernels that reduce quarters separately), then the fp32 partials.
+constexpr size_t kTicketBytes = size_t(((1 << 24) + kRB - 1) / kRB) * 4 * 4;
 static_assert(kStageBytes % 1024 == 0, "128-byte swizzle needs 1 KiB-aligned stages");
 static_assert(kUnitCols == 128, "the swizzle pattern assumes 128-byte rows");
 

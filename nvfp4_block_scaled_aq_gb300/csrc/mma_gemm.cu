@@ -284,6 +284,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const int contrib = int(owner_of(unit0 + units - 1, p.total, grid) - own_lo + 1);
       const int jj = int(blockIdx.x - own_lo);
       const int64_t row = rb * kRB + row_local;
+      // Partials are token-major ([row block][contributor][token][128
+      // rows]) so a warp's 32 rows of one token are one coalesced 128-byte
+      // store, and each 32-row quarter has its own ticket: the warp that
+      // takes the quarter's last ticket adds the contributors' partials of
+      // those 32 rows, in contributor order.
+      float *mine = r.partial + (rb * p.max_contrib + jj) * int64_t(a.slots) * kRB + row_local;
 #pragma unroll
       for (int tok = 0; tok < 64; ++tok) {
         if (tok >= m) break;
@@ -292,34 +298,43 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
             p.y[int64_t(tok) * p.n + row] =
                 f32_to_bf16_rn(__fmul_rn(__fmul_rn(d[tok], __ldg(a.g_dec + tok)), gdw));
         } else {
-          r.partial[((rb * p.max_contrib + jj) * kRB + row_local) * a.slots + tok] = d[tok];
+          mine[tok * kRB] = d[tok];
         }
       }
       if (!complete) {
-        // per-warp tickets: the warp that takes the row block's last of
-        // 4 * contrib tickets adds the partials in contributor order
         __syncwarp();
         unsigned last = 0;
         if (lane == 0) {
           __threadfence();
-          last = atomicAdd(&r.tickets[rb], 1u) == unsigned(4 * contrib - 1);
+          last = atomicAdd(&r.tickets[rb * 4 + q], 1u) == unsigned(contrib - 1);
           __threadfence();
         }
         last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (last) {
-          for (int idx = lane; idx < kRB * m; idx += 32) {
-            const int rl = idx / m, token = idx - rl * m;
-            const int64_t rr = rb * kRB + rl;
-            if (rr >= p.n) continue;
-            float s = 0.0f;
-            for (int c = 0; c < contrib; ++c)
-              s = __fadd_rn(s, __ldcg(r.partial + ((rb * p.max_contrib + c) * kRB + rl) * a.slots + token));
-            p.y[int64_t(token) * p.n + rr] =
-                f32_to_bf16_rn(__fmul_rn(__fmul_rn(s, __ldg(a.g_dec + token)), gdw));
+        if (last && row < p.n) {
+          // contributor by contributor, all tokens' loads in flight at once
+          const float *base = r.partial + rb * p.max_contrib * int64_t(a.slots) * kRB + row_local;
+          const int64_t cstride = int64_t(a.slots) * kRB;
+          for (int t0 = 0; t0 < m; t0 += 16) {
+            float acc[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+            for (int c = 0; c < contrib; ++c) {
+              float v[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                v[i] = t0 + i < m ? __ldcg(base + c * cstride + (t0 + i) * kRB) : 0.0f;
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], v[i]);
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              if (t0 + i < m)
+                p.y[int64_t(t0 + i) * p.n + row] =
+                    f32_to_bf16_rn(__fmul_rn(__fmul_rn(acc[i], __ldg(a.g_dec + t0 + i)), gdw));
           }
-          __syncwarp();
-          if (lane == 0) r.tickets[rb] = 0;
         }
+        __syncwarp();
+        if (last && lane == 0) r.tickets[rb * 4 + q] = 0;
       }
       u += uk1 - uk0;
     }
