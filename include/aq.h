@@ -241,6 +241,8 @@ AQ_API aq_status aq_gemv_nvfp4_noalloc(const aq_nvfp4_weight *w, const uint16_t 
 #define AQ_STEP_PDL 1u /* programmatic dependent launch between projections */
 #define AQ_STEP_REGDECODE 2u /* every projection on the register-decode kernel  */
 #define AQ_STEP_TCGEN05 4u   /* the tcgen05 kernel wherever it serves the shape  */
+#define AQ_STEP_MMA 8u       /* every projection on the block-scaled MMA path:
+                                activations quantised to NVFP4 per row       */
 
 /* One decode step's weight stream: for p = 0 .. n_proj-1 in order,
  * y[p] = GEMV(w[p], x[p]) with m tokens, all on one stream, one launch per

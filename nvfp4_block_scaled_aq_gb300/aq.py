@@ -31,6 +31,7 @@ PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_GEMV_REGDECODE, PATH_GEMV_TCGEN05 = 0, 1, 2
 STEP_PDL = 1
 STEP_REGDECODE = 2
 STEP_TCGEN05 = 4
+STEP_MMA = 8
 MAX_M = 16
 MAX_M_MMA = 64
 NOALLOC_MAX_SCRATCH = 8 << 20  # AQ_GEMV_NOALLOC_MAX_SCRATCH

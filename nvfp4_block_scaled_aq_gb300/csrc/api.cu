@@ -304,13 +304,15 @@ aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,
   if (n_proj < 0) return set_error(AQ_ERR_INVALID_ARG, "%s: n_proj < 0", what);
   if (n_proj == 0) return AQ_OK;
   if (!w || !x || !y) return set_error(AQ_ERR_INVALID_ARG, "%s: w, x, y must not be NULL", what);
-  if (flags & ~(AQ_STEP_PDL | AQ_STEP_REGDECODE | AQ_STEP_TCGEN05))
+  if (flags & ~(AQ_STEP_PDL | AQ_STEP_REGDECODE | AQ_STEP_TCGEN05 | AQ_STEP_MMA))
     return set_error(AQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", what, flags);
-  if ((flags & AQ_STEP_REGDECODE) && (flags & AQ_STEP_TCGEN05))
+  const uint32_t kernels = flags & (AQ_STEP_REGDECODE | AQ_STEP_TCGEN05 | AQ_STEP_MMA);
+  if (kernels & (kernels - 1))
     return set_error(AQ_ERR_INVALID_ARG, "%s: at most one kernel flag", what);
   // Validate every projection before the first launch.
   for (int32_t p = 0; p < n_proj; ++p) {
-    aq_status s = gemv_args(&w[p], x[p], m, y[p], AQ_PATH_GEMV, what);
+    aq_status s = gemv_args(&w[p], x[p], m, y[p],
+                            (flags & AQ_STEP_MMA) ? AQ_PATH_MMA : AQ_PATH_GEMV, what);
     if (s != AQ_OK) {
       char msg[sizeof t_err];
       std::strncpy(msg, t_err, sizeof msg - 1);
@@ -321,14 +323,21 @@ aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,
   const DeviceInfo *dev = device_info();
   if (!dev) return AQ_ERR_UNSUPPORTED;
   for (int32_t p = 0; p < n_proj; ++p) {
-    aq_status s = check_ws(workspace, workspace_bytes, gemv_workspace_bytes(w[p].n, w[p].k, *dev), what);
+    const size_t need = (flags & AQ_STEP_MMA) ? mma_workspace(w[p].n, w[p].k, m, *dev).bytes
+                                              : gemv_workspace_bytes(w[p].n, w[p].k, *dev);
+    aq_status s = check_ws(workspace, workspace_bytes, need, what);
     if (s != AQ_OK) return s;
+    if ((flags & AQ_STEP_MMA) && !mma_eligible(w[p].n, w[p].k, m, *dev))
+      return set_error(AQ_ERR_UNSUPPORTED, "%s: projection %d: the MMA path does not serve m = %d",
+                       what, p, m);
   }
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool pdl = (flags & AQ_STEP_PDL) != 0;
   for (int32_t p = 0; p < n_proj; ++p) {
     cudaError_t e;
-    if (flags & AQ_STEP_REGDECODE)
+    if (flags & AQ_STEP_MMA)
+      e = launch_mma(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
+    else if (flags & AQ_STEP_REGDECODE)
       e = launch_gemv_regdecode(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
     else if ((flags & AQ_STEP_TCGEN05) && tc_eligible(w[p].n, w[p].k, m, *dev))
       e = launch_gemv_tc(w[p], x[p], m, y[p], workspace, pdl, *dev, st);

@@ -14,8 +14,8 @@
 // kind::mxf4nvf4 MMAs (M = 128, K = 64) of the unit into an fp32
 // accumulator; four epilogue warps scale by g_dec_w * g_dec_x[t], round to
 // bf16, and combine split-K partials deterministically (ticket per row
-// block, partials added in contributor order).  One persistent CTA per SM,
-// stream-K ranges of units exactly as the GEMV kernels.  Every wait is
+// quarter, partials added in contributor order).  Two persistent CTAs per
+// SM, stream-K ranges of units exactly as the register-decode GEMV.  Every wait is
 // bounded.
 #include <cudaTypedefs.h>
 
@@ -33,7 +33,10 @@ namespace {
 constexpr int kMmaThreads = 320;  // producer, MMA, 4 scale warps, 4 epilogue warps
 constexpr int kMmaMaxStages = 8;
 constexpr int kMmaMinStages = 3;
-constexpr int kMmaSmem = 227 * 1024;
+// Two CTAs per SM: two independent TMA streams per SM keep HBM far busier
+// than one (pure streaming of these boxes: ~6.3 TB/s with two, ~4.4 with
+// one, whatever the depth).
+constexpr int kMmaSmem = 113 * 1024;
 constexpr int kWarpEpi = 6;
 // tensor memory: accumulators 2 x 64 columns, weight-scale sets 2 x 16,
 // activation-scale sets 2 x 16 (alternate units; copies and MMAs run in
@@ -89,7 +92,7 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t *bar, unsigned parity, vo
   return false;
 }
 
-__global__ void __launch_bounds__(kMmaThreads, 1)
+__global__ void __launch_bounds__(kMmaThreads, 2)
     mma_gemm_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_s,
                     const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xs,
                     Proj p, const Run r, const ActQ a) {
@@ -257,27 +260,6 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       const int uk1 = int(uk0 + (u_end - u) < units ? uk0 + (u_end - u) : units);
       const bool ok = wait_or_abort(&ct.accfull[buf], unsigned(uses[buf]) & 1u, aborted, r.status);
       tcx::fence_after_sync();
-      float d[64];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (c * 16 < N) {
-          uint32_t h16[16];
-          tcx::ld_x16(lane_base + buf * kAccCols + 16 * c, h16);
-          tcx::wait_ld();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) d[16 * c + i] = __uint_as_float(h16[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) d[16 * c + i] = 0.0f;
-        }
-      }
-      tcx::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ct.accempty[buf]);
-      ++uses[buf];
-      buf ^= 1;
-      if (!ok) break;
-
       const bool complete = (uk0 == 0 && uk1 == units);
       const int64_t unit0 = rb * units;
       const int64_t own_lo = owner_of(unit0, p.total, grid);
@@ -288,19 +270,34 @@ __global__ void __launch_bounds__(kMmaThreads, 1)
       // rows]) so a warp's 32 rows of one token are one coalesced 128-byte
       // store, and each 32-row quarter has its own ticket: the warp that
       // takes the quarter's last ticket adds the contributors' partials of
-      // those 32 rows, in contributor order.
+      // those 32 rows, in contributor order.  The accumulator is read 16
+      // tokens at a time.
       float *mine = r.partial + (rb * p.max_contrib + jj) * int64_t(a.slots) * kRB + row_local;
+      for (int c0 = 0; c0 < N; c0 += 16) {
+        uint32_t h16[16];
+        tcx::ld_x16(lane_base + buf * kAccCols + c0, h16);
+        tcx::wait_ld();
+        if (!ok) continue;
 #pragma unroll
-      for (int tok = 0; tok < 64; ++tok) {
-        if (tok >= m) break;
-        if (complete) {
-          if (row < p.n)
-            p.y[int64_t(tok) * p.n + row] =
-                f32_to_bf16_rn(__fmul_rn(__fmul_rn(d[tok], __ldg(a.g_dec + tok)), gdw));
-        } else {
-          mine[tok * kRB] = d[tok];
+        for (int i = 0; i < 16; ++i) {
+          const int tok = c0 + i;
+          if (tok >= m) break;
+          const float v = __uint_as_float(h16[i]);
+          if (complete) {
+            if (row < p.n)
+              p.y[int64_t(tok) * p.n + row] =
+                  f32_to_bf16_rn(__fmul_rn(__fmul_rn(v, __ldg(a.g_dec + tok)), gdw));
+          } else {
+            mine[tok * kRB] = v;
+          }
         }
       }
+      tcx::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ct.accempty[buf]);
+      ++uses[buf];
+      buf ^= 1;
+      if (!ok) break;
       if (!complete) {
         __syncwarp();
         unsigned last = 0;
@@ -366,7 +363,7 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 // mma_n(m) >= 16 token slots, then the quantised activations (packed,
 // scales, g_dec), each 256-byte aligned.
 MmaWorkspace mma_workspace(int n, int k, int m, const DeviceInfo &dev) {
-  const GemvPlan p = plan_gemv_tc(n, k, dev);
+  const GemvPlan p = plan_gemv(n, k, dev);
   MmaWorkspace w;
   w.slots = mma_n(m) < 16 ? 16 : mma_n(m);
   w.scale_pitch = (k / 16 + 15) / 16 * 16;
@@ -396,7 +393,7 @@ cudaError_t launch_mma(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint1
   cudaError_t e = launch_act_quant(x, m, w.k, xq, xs, lay.scale_pitch, xg, dev, st);
   if (e != cudaSuccess) return e;
 
-  const GemvPlan plan = plan_gemv_tc(w.n, w.k, dev);
+  const GemvPlan plan = plan_gemv(w.n, w.k, dev);
   const int N = mma_n(m);
   CUtensorMap tm_w, tm_s, tm_x, tm_xs;
   if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;

@@ -167,3 +167,29 @@ def test_persistent_step_rejects_mismatched_run_on_device():
     assert aq.poll_device_status() == aq.ERR_INVALID_ARG
     aq.step_run(plan, wsp)
     assert aq.poll_device_status() == aq.OK
+
+
+@pytest.mark.parametrize("flag", ["regdecode", "tcgen05", "mma"])
+def test_step_kernel_flags_match_their_single_calls(flag):
+    """aq_decode_step_weights with a kernel flag gives, projection by
+    projection, exactly the single call on that kernel's path."""
+    m = 2
+    Ws, ws, xs, ys = build_stack(2, inputs.LAYER_1B, m, seed=15)
+    fl = {"regdecode": aq.STEP_REGDECODE, "tcgen05": aq.STEP_TCGEN05, "mma": aq.STEP_MMA}[flag]
+    path = {"regdecode": aq.PATH_GEMV_REGDECODE, "tcgen05": aq.PATH_GEMV_TCGEN05,
+            "mma": aq.PATH_MMA}[flag]
+    size = max(aq.gemv_workspace_bytes(n, k, m) for n, k in inputs.LAYER_1B)
+    wsp = torch.zeros(size, dtype=torch.uint8, device=DEV)
+    aq.decode_step(aq.StepArgs(ws, xs, ys), wsp, flags=aq.STEP_PDL | fl)
+    torch.cuda.synchronize()
+    for w, x, y in zip(ws, xs, ys):
+        assert torch.equal(y, gemv_gpu(w, x, path=path))
+    assert aq.poll_device_status() == aq.OK
+
+
+def test_step_rejects_two_kernel_flags():
+    Ws, ws, xs, ys = build_stack(1, inputs.LAYER_1B[:1], 1, seed=16)
+    wsp = step_workspace(inputs.LAYER_1B[:1], 1)
+    with pytest.raises(aq.AqError) as e:
+        aq.decode_step(aq.StepArgs(ws, xs, ys), wsp, flags=aq.STEP_REGDECODE | aq.STEP_MMA)
+    assert e.value.status == aq.ERR_INVALID_ARG
