@@ -33,10 +33,11 @@ constexpr int kSmemBudget = 113 * 1024;         // per CTA, so two fit on an SM
 constexpr int kXChunkBudget = 16;               // m * units staged at once (chunked mode)
 constexpr int kTileHalves = 128;                // f16 per staged 128-column tile
 constexpr unsigned kSpinLimit = 1u << 22;
-// Ticket region of fixed size at the start of a GEMV workspace (four 32-bit
-// tickets per row block of the largest legal n: one per 32-row quarter for
-// the kernels that reduce quarters separately), then the fp32 partials.
-constexpr size_t kTicketBytes = size_t(((1 << 24) + kRB - 1) / kRB) * 4 * 4;
+// Ticket region of fixed size at the start of a GEMV workspace (eight
+// 32-bit tickets per row block of the largest legal n: one per 16-row group
+// of the register-decode kernels, or per 32-row quarter of the tcgen05
+// kernels), then the fp32 partials.
+constexpr size_t kTicketBytes = size_t(((1 << 24) + kRB - 1) / kRB) * 8 * 4;
 static_assert(kStageBytes % 1024 == 0, "128-byte swizzle needs 1 KiB-aligned stages");
 static_assert(kUnitCols == 128, "the swizzle pattern assumes 128-byte rows");
 
@@ -486,28 +487,43 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
         }
       }
     if (!complete) {
-      // the barrier orders every warp's partial stores before thread 0's
-      // gpu-scope fence, which publishes them with the ticket increment
-      consumer_sync();
-      if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned ticket = atomicAdd(&r.tickets[rb], 1u);
-        __threadfence();
-        ct.flag = (ticket == unsigned(contrib - 1));
+      // Each warp publishes its own 16 rows: its partial stores, then one
+      // acquire-release ticket per (row block, row group) at gpu scope.  The
+      // warp that takes a row group's last ticket adds that group's partials
+      // from every contributor, all loaded at once and added in contributor
+      // order.  No barrier spans the warps, so none waits for another.
+      __syncwarp();
+      unsigned last = 0;
+      uint32_t *ticket = r.tickets + rb * kRG + rg;
+      if (lane == 0) {
+        unsigned old;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(ticket) : "memory");
+        last = old == unsigned(contrib - 1);
       }
-      consumer_sync();
-      if (ct.flag) {
-        for (int idx = threadIdx.x; idx < kRB * m; idx += kW * 32) {
-          const int row_local = idx / m, token = idx - row_local * m;
+      last = __shfl_sync(0xFFFFFFFFu, last, 0);
+      __syncwarp();  // every lane's loads below follow lane 0's acquire
+      if (last) {
+        const int64_t qs = int64_t(kRB) * 16;
+        for (int idx = lane; idx < 16 * m; idx += 32) {
+          const int row_local = rg * 16 + idx / m, token = idx % m;
           const int64_t row = rb * kRB + row_local;
           if (row >= p.n) continue;
+          const float *src = r.partial + (rb * p.max_contrib * kRB + row_local) * 16 + token;
           float s = 0.0f;
-          for (int q = 0; q < contrib; ++q)
-            s = __fadd_rn(s, __ldcg(r.partial + ((rb * p.max_contrib + q) * kRB + row_local) * 16 +
-                                    token));
+          if (contrib <= 16) {
+            float v[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) v[q] = q < contrib ? __ldcg(src + q * qs) : 0.0f;
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              if (q < contrib) s = __fadd_rn(s, v[q]);
+          } else {
+            for (int q = 0; q < contrib; ++q) s = __fadd_rn(s, __ldcg(src + q * qs));
+          }
           p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(s, gd));
         }
-        if (threadIdx.x == 0) r.tickets[rb] = 0;
+        __syncwarp();
+        if (lane == 0) *ticket = 0;
       }
     }
     u += uk1 - uk0;
