@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     return;
   }
+  prefetch_x_l2(p, r.m);
   pdl_wait();  // x and the workspace may come from the previous kernel
   consume<NT>(p, r, sv.base, ct, sv.xs, pos, aborted);
 }

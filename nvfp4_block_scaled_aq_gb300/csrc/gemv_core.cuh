@@ -303,6 +303,32 @@ __device__ __forceinline__ void drain(Ctrl &ct, int S, int64_t issued) {
     mbar_wait(&ct.full[j % S], unsigned(j / S) & 1u, &never);
 }
 
+// Pull the activation lines this CTA will stage into L2 ahead of the wait
+// for the previous kernel (or projection): a prefetch reads nothing into the
+// computation, and L2 stays coherent with any later write to x, so it is
+// safe before the wait and takes the HBM latency off the staging after it.
+__device__ __forceinline__ void prefetch_x_l2(const Proj &p, int m) {
+  const int64_t grid = p.grid;
+  if (int64_t(blockIdx.x) >= grid) return;
+  const int64_t u_begin = range_begin(blockIdx.x, p.total, grid);
+  const int64_t u_end = range_begin(blockIdx.x + 1, p.total, grid);
+  if (u_begin >= u_end) return;
+  const int units = p.units;
+  const int64_t L = u_end - u_begin;
+  const bool all_units = L >= units;
+  const int uk_begin = int(u_begin % units);
+  const int slots = x_slots(L, units);
+  const int lines = m * slots * 4;  // 128-byte lines (64 bf16) per 256-column slot
+  for (int i = threadIdx.x; i < lines; i += kW * 32) {
+    const int tok = i / (slots * 4), rem = i - tok * slots * 4;
+    const int s = rem >> 2, q = rem & 3;
+    const int uk = all_units ? s : (uk_begin + s) % units;
+    const int kk = uk * kUnitK + q * 64;
+    if (kk < p.k)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.x + int64_t(tok) * p.k + kk));
+  }
+}
+
 // Consumers: the whole of this CTA's share of projection p -- activation
 // staging, the unit loop, and the split-K epilogue.  Called by the kW
 // consumer warps only.
@@ -349,14 +375,28 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
     for (int tok = 0; tok < m; ++tok) {
       const uint16_t *xrow = p.x + int64_t(tok) * p.k;
       uint32_t mx = 0;
-      for (int v = threadIdx.x; v < nv; v += kW * 32) {
-        const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
-        const int uk = all_units ? s : (uk_begin + s) % units;
-        const int kk = uk * kUnitK + within;
-        uint4 q = make_uint4(0, 0, 0, 0);
-        if (kk < p.k) q = __ldg(reinterpret_cast<const uint4 *>(xrow + kk));
-        mx = absmax8(mx, q);
-        if (full) *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) = q;
+      // four vectors per thread per round, every load issued before any
+      // shared-memory store (the stores go through generic pointers, which
+      // would otherwise keep each load waiting for the previous store)
+      constexpr int kV = 4;
+      for (int v0 = threadIdx.x; v0 < nv; v0 += kV * kW * 32) {
+        uint4 q[kV];
+#pragma unroll
+        for (int i = 0; i < kV; ++i) {
+          const int v = v0 + i * kW * 32;
+          const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
+          const int uk = all_units ? s : (uk_begin + s) % units;
+          const int kk = uk * kUnitK + within;
+          q[i] = make_uint4(0, 0, 0, 0);
+          if (v < nv && kk < p.k) q[i] = __ldg(reinterpret_cast<const uint4 *>(xrow + kk));
+        }
+#pragma unroll
+        for (int i = 0; i < kV; ++i) {
+          const int v = v0 + i * kW * 32;
+          if (v >= nv) break;
+          mx = absmax8(mx, q[i]);
+          if (full) *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) = q[i];
+        }
       }
       mx = max(mx & 0xFFFFu, mx >> 16);
 #pragma unroll
