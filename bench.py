@@ -40,11 +40,11 @@ NOMINAL_HBM_GBS = 8000.0  # the 8 TB/s denominator the metric names
 # capture), keyed by the workload and the sha1 of the GEMV kernel sources the
 # capture was taken on; when they change the figure no longer applies (null).
 NCU_TRAFFIC = {
-    # four launches of layer 0, m = 1: 27,710,208 + 15,107,840 + 137,514,752
-    # + 67,917,056 bytes (profiles/gemv_kernel_31b_layer_dram_traffic.md);
-    # the key is of the sources after a host-only launcher was added to
-    # gemv.cu, the device code of gemv_kernel unchanged
-    ("gemma4-31b-shaped decode-step weight stream", 1, "7c94e0fbd4d71f71277f870b74eb43bf0b53a652"): 248249856,
+    # four launches of layer 0, m = 1: 27,715,328 + 15,111,168 + 137,556,480
+    # + 67,927,552 bytes (profiles/gemv_kernel_31b_layer_dram_traffic.md);
+    # the key is of the sources after the ticket count per row block became a
+    # named host constant, the device code of gemv_kernel unchanged
+    ("gemma4-31b-shaped decode-step weight stream", 1, "c54c5cf063bcddeec599485d47d42ca4f003b1b6"): 248310528,
 }
 
 
@@ -64,6 +64,9 @@ def parse():
     p.add_argument("--sweep-m", type=str, default="",
                    help="comma-separated subset of the sweep's M values (profiling)")
     p.add_argument("--sweep-proj", choices=("both", "gate_up", "down"), default="both")
+    p.add_argument("--kernel", choices=("regdecode", "tcgen05"), default="regdecode",
+                   help="GEMV kernel of the timed step (regdecode: the library's default "
+                        "for m <= 16; the other one is timed among the extras)")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the eager / no-PDL / end-to-end / CPU-baseline legs")
     return p.parse_args()
@@ -371,15 +374,11 @@ def run_aq(a, dist):
         aq.step_run(stack.plan, stack.plan_ws, stream=stream)
 
     # the timed path: one GEMV launch per projection (PDL), captured in a
-    # graph, on the kernel that is faster for this stack (both are timed)
-    kernel_ms = {}
-    for kname, kflag in (("regdecode", aq.STEP_REGDECODE), ("tcgen05", aq.STEP_TCGEN05)):
-        g = capture(stack, aq.STEP_PDL | kflag, stream)
-        kernel_ms[kname] = time_region(replay(g), max(3, a.steps // 4), a.warmup, stream, dist) \
-            / max(3, a.steps // 4) * 1e3
-        del g
-    kernel = min(kernel_ms, key=kernel_ms.get)
-    kflag = aq.STEP_REGDECODE if kernel == "regdecode" else aq.STEP_TCGEN05
+    # graph, on the kernel chosen by --kernel (the library's default unless
+    # asked otherwise: fixed, so a profiler's launch list sees the same legs)
+    flags = {"regdecode": aq.STEP_REGDECODE, "tcgen05": aq.STEP_TCGEN05}
+    kernel = a.kernel
+    kflag = flags[kernel]
     g_pdl = capture(stack, aq.STEP_PDL | kflag, stream)
     sampler = ClockSampler(dist.local) if dist.rank == 0 else None
     time.sleep(0.3 if sampler else 0)
@@ -389,10 +388,17 @@ def run_aq(a, dist):
     ms = secs / a.steps * 1e3
     value = dist.world * step_bytes * a.steps / secs / 1e9
 
-    extras = {"kernel": kernel,
-              "graph_pdl_ms_per_step_by_kernel": {k: round(v, 4) for k, v in kernel_ms.items()}}
+    extras = {"kernel": kernel}
     e2e = None
     if not a.no_extras:
+        kernel_ms = {kernel: ms}
+        for kname, fl in flags.items():
+            if kname != kernel:
+                g = capture(stack, aq.STEP_PDL | fl, stream)
+                kernel_ms[kname] = time_region(replay(g), a.steps, a.warmup, stream, dist) \
+                    / a.steps * 1e3
+                del g
+        extras["graph_pdl_ms_per_step_by_kernel"] = {k: round(v, 4) for k, v in kernel_ms.items()}
         extras["persistent_step_run_ms_per_step"] = round(
             time_region(persistent, a.steps, a.warmup, stream, dist) / a.steps * 1e3, 4)
         g_nopdl = capture(stack, kflag, stream)

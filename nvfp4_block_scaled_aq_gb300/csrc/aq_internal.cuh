@@ -198,6 +198,9 @@ struct GemvPlan {
   int grid;            // persistent CTAs
   int max_contrib;     // most CTAs sharing one row block
 };
+// Split-K tickets per row block at the start of a GEMV workspace (one per
+// 16-row group of the register-decode kernel).
+constexpr int kTicketsPerRowBlock = 8;
 GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev);
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev);
 cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,

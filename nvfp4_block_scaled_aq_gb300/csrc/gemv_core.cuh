@@ -37,7 +37,8 @@ constexpr unsigned kSpinLimit = 1u << 22;
 // 32-bit tickets per row block of the largest legal n: one per 16-row group
 // of the register-decode kernels, or per 32-row quarter of the tcgen05
 // kernels), then the fp32 partials.
-constexpr size_t kTicketBytes = size_t(((1 << 24) + kRB - 1) / kRB) * 8 * 4;
+constexpr size_t kTicketBytes = size_t(((1 << 24) + kRB - 1) / kRB) * kTicketsPerRowBlock * 4;
+static_assert(kTicketsPerRowBlock == kRG, "one ticket per row group");
 static_assert(kStageBytes % 1024 == 0, "128-byte swizzle needs 1 KiB-aligned stages");
 static_assert(kUnitCols == 128, "the swizzle pattern assumes 128-byte rows");
 

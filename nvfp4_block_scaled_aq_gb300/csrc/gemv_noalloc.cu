@@ -81,7 +81,8 @@ aq_status aq_gemv_nvfp4_noalloc(const aq_nvfp4_weight *w, const uint16_t *x, int
   // zero, but one that gave up on a bounded wait may not, so the tickets of
   // this weight's row blocks are cleared on the stream before every launch;
   // the partial sums are always written before they are read.
-  const size_t tickets = size_t(plan_gemv(w->n, w->k, *dev).row_blocks) * sizeof(uint32_t);
+  const size_t tickets =
+      size_t(plan_gemv(w->n, w->k, *dev).row_blocks) * kTicketsPerRowBlock * sizeof(uint32_t);
   cudaError_t e = cudaMemsetAsync(scratch, 0, tickets, st);
   if (e != cudaSuccess) return cuda_error(e, what);
   e = launch_gemv_uncached(*w, x, m, y, scratch, *dev, st);
