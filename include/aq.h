@@ -171,7 +171,9 @@ typedef enum {
  * MMA path it also holds the quantised activations).  It must be
  * ZERO-FILLED once after allocation; every call leaves it in the state it
  * needs next, so one zeroed workspace serves any sequence of calls on one
- * stream.  Calls that may run concurrently need separate workspaces. */
+ * stream.  Calls that may run concurrently need separate workspaces.  A
+ * call after which aq_poll_device_status reports AQ_ERR_TIMEOUT may leave
+ * it dirty: zero-fill it again before the next call. */
 AQ_API size_t aq_gemv_workspace_bytes(int32_t n, int32_t k, int32_t m);
 
 /* y[t, i] = bf16( sum_k x[t, k] * w_hat[i, k] ), w_hat = e2m1(q)*sd*g_dec,

@@ -334,15 +334,18 @@ aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const bool pdl = (flags & AQ_STEP_PDL) != 0;
   for (int32_t p = 0; p < n_proj; ++p) {
+    // the register-decode kernel pulls the next projection's first weight
+    // units into L2 while its own launch drains
+    const aq_nvfp4_weight *next = p + 1 < n_proj ? &w[p + 1] : nullptr;
     cudaError_t e;
     if (flags & AQ_STEP_MMA)
       e = launch_mma(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
     else if (flags & AQ_STEP_REGDECODE)
-      e = launch_gemv_regdecode(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
+      e = launch_gemv_regdecode(w[p], x[p], m, y[p], workspace, pdl, *dev, st, next);
     else if ((flags & AQ_STEP_TCGEN05) && tc_eligible(w[p].n, w[p].k, m, *dev))
       e = launch_gemv_tc(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
     else
-      e = launch_gemv(w[p], x[p], m, y[p], workspace, pdl, *dev, st);
+      e = launch_gemv(w[p], x[p], m, y[p], workspace, pdl, *dev, st, next);
     if (e != cudaSuccess) return cuda_error(e, what);
   }
   return AQ_OK;

@@ -203,8 +203,11 @@ struct GemvPlan {
 constexpr int kTicketsPerRowBlock = 8;
 GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev);
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev);
+// `next`, when given, is the projection launched after this one on the same
+// stream: the kernel prefetches the first weight units of it into L2.
 cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
-                        void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st);
+                        void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st,
+                        const aq_nvfp4_weight *next = nullptr);
 // The tcgen05 kernel (tc_gemv.cu): its plan, whether it serves a shape for
 // m tokens, its workspace, and its launch.
 GemvPlan plan_gemv_tc(int n, int k, const DeviceInfo &dev);
@@ -231,7 +234,7 @@ bool encode_act_maps(const uint8_t *xq, const uint8_t *xs, int m, int k, int sca
 // Register-decode kernel only (gemv.cu).
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
-                                  cudaStream_t st);
+                                  cudaStream_t st, const aq_nvfp4_weight *next = nullptr);
 cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                  uint16_t *y, void *ws, const DeviceInfo &dev,
                                  cudaStream_t st);

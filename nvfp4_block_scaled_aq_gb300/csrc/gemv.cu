@@ -57,13 +57,17 @@ namespace {
 template <int NT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gemv_kernel(const __grid_constant__ CUtensorMap tm_w,
-                const __grid_constant__ CUtensorMap tm_s, Proj p, const Run r) {
+                const __grid_constant__ CUtensorMap tm_s,
+                const __grid_constant__ CUtensorMap tm_nw,
+                const __grid_constant__ CUtensorMap tm_ns, Proj p, const Run r) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const SmemView sv = carve(smem_raw, r.stages);
   Ctrl &ct = *sv.ct;
   volatile int *aborted = &ct.aborted;
   p.tm_w = &tm_w;
   p.tm_s = &tm_s;
+  p.nx_w = &tm_nw;
+  p.nx_s = &tm_ns;
   if (threadIdx.x == 0) {
     init_ring(ct, r.stages);
     pdl_launch_dependents();
@@ -74,7 +78,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if ((threadIdx.x & 31) == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s)) : "memory");
-      produce(p, sv.base, ct, r.stages, pos, aborted, r.status);
+      if (produce(p, sv.base, ct, r.stages, pos, aborted, r.status)) prefetch_next(p);
       drain(ct, r.stages, pos.count);
     }
     return;
@@ -248,17 +252,18 @@ size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev) {
 // today, so it serves every m unless the tcgen05 kernel is asked for.
 constexpr bool kAutoPrefersTc = false;
 cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
-                        void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st) {
+                        void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st,
+                        const aq_nvfp4_weight *next) {
   if (kAutoPrefersTc && tc_eligible(w.n, w.k, m, dev))
     return launch_gemv_tc(w, x, m, y, ws, pdl, dev, st);
-  return launch_gemv_regdecode(w, x, m, y, ws, pdl, dev, st);
+  return launch_gemv_regdecode(w, x, m, y, ws, pdl, dev, st, next);
 }
 
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, const aq_nvfp4_weight *next) {
   const GemvPlan plan = plan_gemv(w.n, w.k, dev);
-  CUtensorMap tm_w, tm_s;
+  CUtensorMap tm_w, tm_s, tm_nw, tm_ns;
   if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
 
   Run r;
@@ -283,6 +288,20 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   p.units = int(plan.units);
   p.max_contrib = plan.max_contrib;
   p.grid = plan.grid;
+  p.nx_w = p.nx_s = nullptr;
+  p.nx_total = 0;
+  p.nx_units = p.nx_grid = p.nx_pf = 0;
+  if (next) {
+    if (!encode_maps(*next, &tm_nw, &tm_ns)) return cudaErrorInvalidValue;
+    const GemvPlan np = plan_gemv(next->n, next->k, dev);
+    p.nx_total = np.total;
+    p.nx_units = int(np.units);
+    p.nx_grid = np.grid;
+    p.nx_pf = kPrefetchUnits;
+  } else {
+    tm_nw = tm_w;  // unused
+    tm_ns = tm_s;
+  }
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
@@ -297,10 +316,10 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   cudaError_t e;
   if (m <= 8) {
     if ((e = set_smem_attr<1>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1>, tm_w, tm_s, p, r);
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1>, tm_w, tm_s, tm_nw, tm_ns, p, r);
   } else {
     if ((e = set_smem_attr<2>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2>, tm_w, tm_s, p, r);
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2>, tm_w, tm_s, tm_nw, tm_ns, p, r);
   }
   return e;
 }
@@ -342,6 +361,9 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   p.units = int(plan.units);
   p.max_contrib = plan.max_contrib;
   p.grid = plan.grid;
+  p.nx_w = p.nx_s = nullptr;  // no prefetch of a next projection
+  p.nx_total = 0;
+  p.nx_units = p.nx_grid = p.nx_pf = 0;
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
@@ -351,10 +373,10 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   cudaError_t e;
   if (m <= 8) {
     if ((e = set_smem_attr<1>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1>, tm_w, tm_s, p, r);
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1>, tm_w, tm_s, tm_w, tm_s, p, r);
   } else {
     if ((e = set_smem_attr<2>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2>, tm_w, tm_s, p, r);
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2>, tm_w, tm_s, tm_w, tm_s, p, r);
   }
   return e;
 }

@@ -100,6 +100,20 @@ __device__ __forceinline__ Proj to_proj(const StepProj &s) {
   p.units = s.units;
   p.max_contrib = s.max_contrib;
   p.grid = s.grid;
+  p.nx_w = p.nx_s = nullptr;
+  p.nx_total = 0;
+  p.nx_units = p.nx_grid = p.nx_pf = 0;
+  return p;
+}
+
+// Projection s with the L2 prefetch of projection n's first units.
+__device__ __forceinline__ Proj with_next(Proj p, const StepProj &n) {
+  p.nx_w = &n.tm_w;
+  p.nx_s = &n.tm_s;
+  p.nx_total = n.total;
+  p.nx_units = n.units;
+  p.nx_grid = n.grid;
+  p.nx_pf = kPrefetchUnits;
   return p;
 }
 
@@ -132,8 +146,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
   if ((threadIdx.x >> 5) == kW) {  // producer warp: every projection, back to back
     if ((threadIdx.x & 31) == 0) {
-      for (int p = 0; p < h.n_proj; ++p)
+      for (int p = 0; p < h.n_proj; ++p) {
         if (!produce(to_proj(projs[p]), sv.base, ct, h.stages, pos, aborted, status)) break;
+        if (p + 1 < h.n_proj) prefetch_next(with_next(to_proj(projs[p]), projs[p + 1]));
+      }
       drain(ct, h.stages, pos.count);
     }
     return;
