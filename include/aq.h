@@ -234,7 +234,7 @@ AQ_API aq_status aq_quantize_act_nvfp4(const uint16_t *x, int32_t m, int32_t k,
  * All calls on a device share the one array, which keeps the last call's
  * contents: calls whose kernels can overlap on the GPU (different streams,
  * different host threads) race on it and must be ordered by the caller. */
-#define AQ_GEMV_NOALLOC_MAX_SCRATCH (16u << 20) /* bytes per device */
+#define AQ_GEMV_NOALLOC_MAX_SCRATCH (32u << 20) /* bytes per device */
 AQ_API aq_status aq_gemv_nvfp4_noalloc(const aq_nvfp4_weight *w, const uint16_t *x,
                                        int32_t m, uint16_t *y, aq_path path,
                                        aq_stream_t stream);

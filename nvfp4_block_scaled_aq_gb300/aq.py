@@ -34,7 +34,7 @@ STEP_TCGEN05 = 4
 STEP_MMA = 8
 MAX_M = 16
 MAX_M_MMA = 64
-NOALLOC_MAX_SCRATCH = 16 << 20  # AQ_GEMV_NOALLOC_MAX_SCRATCH
+NOALLOC_MAX_SCRATCH = 32 << 20  # AQ_GEMV_NOALLOC_MAX_SCRATCH
 
 
 class AqLibraryMissing(RuntimeError):

@@ -242,7 +242,7 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev) {
 // Enough for either kernel, so one workspace serves every token count.
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev) {
   const GemvPlan p = plan_gemv(n, k, dev);
-  const size_t reg = kTicketBytes + size_t(p.row_blocks) * p.max_contrib * kRB * 16 * sizeof(float);
+  const size_t reg = kRestOffset + size_t(p.row_blocks) * p.max_contrib * kRB * 16 * sizeof(float);
   const size_t tc = gemv_tc_workspace_bytes(n, k, dev);
   return reg > tc ? reg : tc;
 }
@@ -266,17 +266,18 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   CUtensorMap tm_w, tm_s, tm_nw, tm_ns;
   if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
 
-  Run r;
+  Run r{};
   uint8_t *wsb = static_cast<uint8_t *>(ws);
   r.tickets = reinterpret_cast<uint32_t *>(wsb);
-  r.partial = reinterpret_cast<float *>(wsb + kTicketBytes);
+  r.zero = reinterpret_cast<uint32_t *>(wsb + kTicketBytes);
+  r.partial = reinterpret_cast<float *>(wsb + kRestOffset);
   r.status = dev.status;
   r.m = m;
   r.x_cap = x_cap_for(plan, m);
   r.stages = stages_for(r.x_cap);
   if (r.stages < kMinStages) return cudaErrorInvalidConfiguration;
 
-  Proj p;
+  Proj p{};
   p.tm_w = nullptr;  // set from the kernel's own parameters
   p.tm_s = nullptr;
   p.g_dec = w.global_scale;
@@ -288,6 +289,7 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   p.units = int(plan.units);
   p.max_contrib = plan.max_contrib;
   p.grid = plan.grid;
+  p.direct = direct_partials_fit(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
   p.nx_w = p.nx_s = nullptr;
   p.nx_total = 0;
   p.nx_units = p.nx_grid = p.nx_pf = 0;
@@ -339,17 +341,18 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   if (!make_map(&tm_s, w.scales, srow, uint64_t(ceil_div(w.n, kTileRows)), kKT * 128, kRG, false))
     return cudaErrorInvalidValue;
 
-  Run r;
+  Run r{};
   uint8_t *wsb = static_cast<uint8_t *>(ws);
   r.tickets = reinterpret_cast<uint32_t *>(wsb);
-  r.partial = reinterpret_cast<float *>(wsb + kTicketBytes);
+  r.zero = reinterpret_cast<uint32_t *>(wsb + kTicketBytes);
+  r.partial = reinterpret_cast<float *>(wsb + kRestOffset);
   r.status = dev.status;
   r.m = m;
   r.x_cap = x_cap_for(plan, m);
   r.stages = stages_for(r.x_cap);
   if (r.stages < kMinStages) return cudaErrorInvalidConfiguration;
 
-  Proj p;
+  Proj p{};
   p.tm_w = nullptr;  // set from the kernel's own parameters
   p.tm_s = nullptr;
   p.g_dec = w.global_scale;
@@ -361,6 +364,7 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   p.units = int(plan.units);
   p.max_contrib = plan.max_contrib;
   p.grid = plan.grid;
+  p.direct = direct_partials_fit(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
   p.nx_w = p.nx_s = nullptr;  // no prefetch of a next projection
   p.nx_total = 0;
   p.nx_units = p.nx_grid = p.nx_pf = 0;

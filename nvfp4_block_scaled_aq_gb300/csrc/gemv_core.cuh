@@ -33,11 +33,20 @@ constexpr int kSmemBudget = 113 * 1024;         // per CTA, so two fit on an SM
 constexpr int kXChunkBudget = 16;               // m * units staged at once (chunked mode)
 constexpr int kTileHalves = 128;                // f16 per staged 128-column tile
 constexpr unsigned kSpinLimit = 1u << 22;
-// Ticket region of fixed size at the start of a GEMV workspace (eight
-// 32-bit tickets per row block of the largest legal n: one per 16-row group
-// of the register-decode kernels, or per 32-row quarter of the tcgen05
-// kernels), then the fp32 partials.
+// Layout of every GEMV workspace:
+//  [0, kTicketBytes)          32-bit tickets, eight per row block of the
+//                             largest legal n (one per 16-row group of the
+//                             register-decode kernel, or per 32-row quarter
+//                             of the tcgen05 kernels);
+//  [kTicketBytes, kRestOffset) the zero region: encoded split-K partials of
+//                             the register-decode kernel, a word of zero
+//                             meaning "not written yet";
+//  [kRestOffset, ...)         the other kernels' partials and buffers.
+// The first two regions are zero between calls: every kernel that writes
+// there puts zeros back before it completes.
 constexpr size_t kTicketBytes = size_t(((1 << 24) + kRB - 1) / kRB) * kTicketsPerRowBlock * 4;
+constexpr size_t kZeroBytes = size_t(8) << 20;
+constexpr size_t kRestOffset = kTicketBytes + kZeroBytes;
 static_assert(kTicketsPerRowBlock == kRG, "one ticket per row group");
 static_assert(kStageBytes % 1024 == 0, "128-byte swizzle needs 1 KiB-aligned stages");
 static_assert(kUnitCols == 128, "the swizzle pattern assumes 128-byte rows");
@@ -92,7 +101,21 @@ struct Proj {
   int nx_units;
   int nx_grid;
   int nx_pf;                // units per CTA to prefetch
+  int direct;               // split-K partials go to the zero region, see
+                            // direct_partials_fit()
 };
+
+// The reducer of a split row block can poll the partials themselves when
+// they are stored encoded in the zero region: [row_blocks][max_contrib - 1]
+// [m][kRB] words of ~bits(partial) (never zero: no fp32 operation yields
+// the all-ones NaN), which it reads, adds and puts back to zero.  Used for
+// m <= 8 (the one-n8-block kernel, where its registers are free) when the
+// words fit the region; the sums are the same either way.
+__host__ __device__ __forceinline__ bool direct_partials_fit(int64_t row_blocks, int max_contrib,
+                                                             int m) {
+  return m <= 8 && max_contrib <= 16 &&
+         size_t(row_blocks) * size_t(max_contrib - 1) * size_t(m) * kRB * 4 <= kZeroBytes;
+}
 
 // Units of the next projection each CTA prefetches into L2 once its own
 // loads are issued (4 x 18 KiB on each of 304 CTAs, 22 MB).  Measured on the
@@ -103,7 +126,8 @@ constexpr int kPrefetchUnits = 4;
 // Per-launch state.
 struct Run {
   float *partial;           // [row_blocks][max_contrib][kRB][16]
-  uint32_t *tickets;        // [row_blocks]
+  uint32_t *tickets;        // [row_blocks][kRG]
+  uint32_t *zero;           // the zero region (encoded partials)
   unsigned *status;
   int m;
   int stages;
@@ -550,15 +574,19 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
     const int contrib = int(owner_of(unit0 + units - 1, p.total, grid) - own_lo + 1);
     const int jj = int(blockIdx.x - own_lo);
     // Split row blocks: contributor 0 (the CTA whose range ends in this row
-    // block, so usually among the last to finish it) reduces; the others
-    // store their partials and publish them with one release-add per
-    // (row block, row group) that nobody waits on.  The reducer keeps its
-    // own partial in registers, waits (bounded) until the count of
-    // published contributors is complete, then adds the partials in
-    // contributor order and clears the count.  No barrier spans the warps.
-    uint32_t *flag = r.tickets + rb * kRG + rg;
+    // block, so usually among the last to finish it) reduces, keeping its
+    // own partial in registers and adding the others' in contributor order;
+    // no barrier spans the warps, and no other contributor waits.
+    //  * direct: the others store ~bits(partial) to the zero region and
+    //    leave; the reducer polls those words (bounded) until none is zero,
+    //    then puts the zeros back.
+    //  * otherwise: the others store plain partials and publish them with
+    //    one release-add per (row block, row group); the reducer waits
+    //    (bounded) for the count, reads the partials and clears the count.
     const bool reducer = !complete && jj == 0;
+    const bool direct = NT == 1 && p.direct;
     float vown[NT][4];
+    const int64_t zrow = (rb * (p.max_contrib - 1) - 1) * m;  // + (j * m + token) * kRB + row
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -569,16 +597,73 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
         const float v = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[min(token, 15)]);
         vown[nt][i] = v;
         if (token >= m || row >= p.n) continue;
-        if (complete)
+        if (complete) {
           p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(v, gd));
-        else if (!reducer)
-          r.partial[((rb * p.max_contrib + jj) * kRB + row_local) * 16 + token] = v;
+        } else if (!reducer) {
+          if (direct)
+            asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(
+                             r.zero + (zrow + int64_t(jj) * m + token) * kRB + row_local),
+                         "r"(~__float_as_uint(v))
+                         : "memory");
+          else
+            r.partial[((rb * p.max_contrib + jj) * kRB + row_local) * 16 + token] = v;
+        }
       }
-    if (!complete && !reducer) {
+    if (!complete && !reducer && !direct) {
       __syncwarp();  // the warp's partial stores precede lane 0's release
       if (lane == 0)
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(flag) : "memory");
+        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(r.tickets + rb * kRG + rg)
+                     : "memory");
+    } else if (reducer && direct) {
+      bool ok = true;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int token = nt * 8 + 2 * c + (i & 1);
+          const int row_local = rg * 16 + g + 8 * (i >> 1);
+          const int64_t row = rb * kRB + row_local;
+          if (!ok || token >= m || row >= p.n) continue;
+          const int64_t at = (zrow + token) * kRB + row_local;  // word of contributor j: at + j * qs
+          const int64_t qs = int64_t(m) * kRB;
+          uint32_t w[16];
+#pragma unroll
+          for (int q = 1; q < 16; ++q) {
+            w[q] = 1u;
+            if (q < contrib)
+              asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w[q]) : "l"(r.zero + (at + q * qs)) : "memory");
+          }
+          for (unsigned it = 0;; ++it) {
+            bool all = true;
+#pragma unroll
+            for (int q = 1; q < 16; ++q) all = all && w[q] != 0u;
+            if (all) break;
+            if (it >= kSpinLimit || *aborted) {
+              ok = false;
+              break;
+            }
+            __nanosleep(32);
+#pragma unroll
+            for (int q = 1; q < 16; ++q)
+              if (q < contrib && w[q] == 0u)
+                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w[q]) : "l"(r.zero + (at + q * qs)) : "memory");
+          }
+          if (!ok) continue;
+          float s = __fadd_rn(0.0f, vown[nt][i]);
+#pragma unroll
+          for (int q = 1; q < 16; ++q)
+            if (q < contrib) {
+              s = __fadd_rn(s, __uint_as_float(~w[q]));
+              asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(r.zero + (at + q * qs)), "r"(0u) : "memory");
+            }
+          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(s, gd));
+        }
+      if (!ok && !*aborted) {
+        *aborted = 1;
+        raise_status(r.status, kDevTimeout);
+      }
     } else if (reducer) {
+      uint32_t *flag = r.tickets + rb * kRG + rg;
       bool ok = true;
       if (lane == 0) {
         const unsigned want = unsigned(contrib - 1);

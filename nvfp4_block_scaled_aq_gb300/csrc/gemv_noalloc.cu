@@ -17,7 +17,7 @@
 #include <cstring>
 #include <mutex>
 
-#include "aq_internal.cuh"
+#include "gemv_core.cuh"
 
 namespace aq {
 namespace {
@@ -77,13 +77,17 @@ aq_status aq_gemv_nvfp4_noalloc(const aq_nvfp4_weight *w, const uint16_t *x, int
   uint8_t *scratch = nullptr;
   if ((s = scratch_for(*dev, &scratch)) != AQ_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-  // The split-K tickets must start at zero.  A completed call leaves them
-  // zero, but one that gave up on a bounded wait may not, so the tickets of
-  // this weight's row blocks are cleared on the stream before every launch;
-  // the partial sums are always written before they are read.
-  const size_t tickets =
-      size_t(plan_gemv(w->n, w->k, *dev).row_blocks) * kTicketsPerRowBlock * sizeof(uint32_t);
+  // The split-K tickets and the encoded partials of the zero region must
+  // start at zero.  A completed call leaves them zero, but one that gave up
+  // on a bounded wait may not, so the part of both that this weight uses is
+  // cleared on the stream before every launch; the plain partials after
+  // them are always written before they are read.
+  const GemvPlan plan = plan_gemv(w->n, w->k, *dev);
+  const size_t tickets = size_t(plan.row_blocks) * kTicketsPerRowBlock * sizeof(uint32_t);
   cudaError_t e = cudaMemsetAsync(scratch, 0, tickets, st);
+  if (e == cudaSuccess && core::direct_partials_fit(plan.row_blocks, plan.max_contrib, m))
+    e = cudaMemsetAsync(scratch + core::kTicketBytes, 0,
+                        size_t(plan.row_blocks) * (plan.max_contrib - 1) * m * core::kRB * 4, st);
   if (e != cudaSuccess) return cuda_error(e, what);
   e = launch_gemv_uncached(*w, x, m, y, scratch, *dev, st);
   return e == cudaSuccess ? AQ_OK : cuda_error(e, what);

@@ -367,7 +367,7 @@ MmaWorkspace mma_workspace(int n, int k, int m, const DeviceInfo &dev) {
   MmaWorkspace w;
   w.slots = mma_n(m) < 16 ? 16 : mma_n(m);
   w.scale_pitch = (k / 16 + 15) / 16 * 16;
-  w.partial_off = kTicketBytes;
+  w.partial_off = kRestOffset;
   w.xq_off = align256(w.partial_off + size_t(p.row_blocks) * p.max_contrib * kRB * w.slots * 4);
   w.xs_off = align256(w.xq_off + size_t(m) * (k / 2));
   w.xg_off = align256(w.xs_off + size_t(m) * w.scale_pitch);
@@ -399,7 +399,7 @@ cudaError_t launch_mma(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint1
   if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
   if (!encode_act_maps(xq, xs, m, w.k, lay.scale_pitch, N, &tm_x, &tm_xs))
     return cudaErrorInvalidValue;
-  Run r;
+  Run r{};
   r.tickets = reinterpret_cast<uint32_t *>(wsb);
   r.partial = reinterpret_cast<float *>(wsb + lay.partial_off);
   r.status = dev.status;
@@ -407,7 +407,7 @@ cudaError_t launch_mma(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint1
   r.stages = mma_stages(N);
   r.x_cap = 0;
   if (r.stages < kMmaMinStages) return cudaErrorInvalidConfiguration;
-  Proj p;
+  Proj p{};
   p.tm_w = nullptr;
   p.tm_s = nullptr;
   p.g_dec = w.global_scale;

@@ -54,6 +54,7 @@ struct alignas(128) StepProj {
   uint16_t *y;
   int64_t total;
   int32_t n, k, units, max_contrib, grid;
+  int32_t direct;      // split-K partials through the zero region
 };
 
 // Grid-wide barrier of the consumer warps (generation counter; the last CTA
@@ -88,7 +89,7 @@ __device__ __forceinline__ void grid_barrier(unsigned *bar, unsigned nblocks,
 }
 
 __device__ __forceinline__ Proj to_proj(const StepProj &s) {
-  Proj p;
+  Proj p{};
   p.tm_w = &s.tm_w;
   p.tm_s = &s.tm_s;
   p.g_dec = s.g_dec;
@@ -100,6 +101,7 @@ __device__ __forceinline__ Proj to_proj(const StepProj &s) {
   p.units = s.units;
   p.max_contrib = s.max_contrib;
   p.grid = s.grid;
+  p.direct = s.direct;
   p.nx_w = p.nx_s = nullptr;
   p.nx_total = 0;
   p.nx_units = p.nx_grid = p.nx_pf = 0;
@@ -135,8 +137,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   if (threadIdx.x == 0) init_ring(ct, h.stages);
   __syncthreads();
 
-  Run r;
+  Run r{};
   r.tickets = reinterpret_cast<uint32_t *>(ws);
+  r.zero = reinterpret_cast<uint32_t *>(ws + kTicketBytes);
   r.partial = reinterpret_cast<float *>(ws + h.partial_off);
   r.status = status;
   r.m = h.m;
@@ -218,6 +221,7 @@ aq_status step_plan_create(const aq_nvfp4_weight *w, int n_proj, const uint16_t 
       if (c > worst) worst = c;
     }
     sp.max_contrib = worst;
+    sp.direct = direct_partials_fit(row_blocks, worst, m) ? 1 : 0;
     const int64_t longest = ceil_div(sp.total, G);
     const int64_t need = int64_t(m) * x_stride_full(x_slots(longest, int(units)));
     if (need * 2 <= kStepXCapBytes && need > x_need) x_need = need;
@@ -229,8 +233,8 @@ aq_status step_plan_create(const aq_nvfp4_weight *w, int n_proj, const uint16_t 
   h.stages = stages_for(h.x_cap);
   if (h.stages < kMinStages)
     return set_error(AQ_ERR_SHAPE, "aq_step_plan_create: activations of m = %d leave no room for the ring", m);
-  h.partial_off = int64_t(kTicketBytes);
-  h.barrier_off = int64_t(kTicketBytes) + (partial_max + 255) / 256 * 256;
+  h.partial_off = int64_t(kRestOffset);
+  h.barrier_off = int64_t(kRestOffset) + (partial_max + 255) / 256 * 256;
   h.ws_required = h.barrier_off + 256;
   std::memcpy(buf.data(), &h, sizeof h);
   if (plan_bytes < buf.size())

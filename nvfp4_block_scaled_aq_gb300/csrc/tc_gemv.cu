@@ -584,7 +584,7 @@ bool tc_eligible(int n, int k, int m, const DeviceInfo &dev) {
 
 size_t gemv_tc_workspace_bytes(int n, int k, const DeviceInfo &dev) {
   const GemvPlan p = plan_gemv_tc(n, k, dev);
-  return kTicketBytes + size_t(p.row_blocks) * p.max_contrib * kRB * 16 * sizeof(float);
+  return kRestOffset + size_t(p.row_blocks) * p.max_contrib * kRB * 16 * sizeof(float);
 }
 
 cudaError_t launch_gemv_tc(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,
@@ -594,17 +594,17 @@ cudaError_t launch_gemv_tc(const aq_nvfp4_weight &w, const uint16_t *x, int m, u
   if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
   const int64_t longest = ceil_div(plan.total, plan.grid);
   const int slots = x_slots(longest, int(plan.units));
-  Run r;
+  Run r{};
   uint8_t *wsb = static_cast<uint8_t *>(ws);
   r.tickets = reinterpret_cast<uint32_t *>(wsb);
-  r.partial = reinterpret_cast<float *>(wsb + kTicketBytes);
+  r.partial = reinterpret_cast<float *>(wsb + kRestOffset);
   r.status = dev.status;
   r.m = m;
   r.stages = tc_stages(slots, tc_n(m));
   r.x_cap = 0;
   if (r.stages < kTcMinStages) return cudaErrorInvalidConfiguration;
 
-  Proj p;
+  Proj p{};
   p.tm_w = nullptr;  // set from the kernel's own parameters
   p.tm_s = nullptr;
   p.g_dec = w.global_scale;

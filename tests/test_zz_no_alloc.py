@@ -53,10 +53,10 @@ def test_noalloc_matches_workspace_gemv_on_consecutive_calls():
 
 
 def test_noalloc_rejects_a_weight_beyond_the_scratch():
-    # [2^17, 1024]: thousands of row blocks, far more partial sums than the
+    # [2^19, 1024]: thousands of row blocks, far more partial sums than the
     # fixed scratch holds.  The buffers are real and full-sized, so the call
     # is rejected on the host with nothing out of bounds even in principle.
-    n, k = 1 << 17, 1024
+    n, k = 1 << 19, 1024
     need = aq.gemv_workspace_bytes(n, k, 1)
     if need <= aq.NOALLOC_MAX_SCRATCH:
         pytest.skip("this device's split needs only %d bytes" % need)
