@@ -428,62 +428,120 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
 
   // -- per-token power-of-two shift from the largest |x| over the staged
   //    columns (a function of the token's own data and the partition only,
-  //    never of m); in full mode the raw bf16 values land in shared memory
-  //    on the same pass and are converted in place afterwards.
-  if (threadIdx.x < 16) ct.xmax[threadIdx.x] = 0;
-  consumer_sync();
-  {
-    const int nv = slots * (kUnitK / 8);
-    for (int tok = 0; tok < m; ++tok) {
-      const uint16_t *xrow = p.x + int64_t(tok) * p.k;
-      uint32_t mx = 0;
-      // four vectors per thread per round, every load issued before any
-      // shared-memory store (the stores go through generic pointers, which
-      // would otherwise keep each load waiting for the previous store)
-      constexpr int kV = 4;
-      for (int v0 = threadIdx.x; v0 < nv; v0 += kV * kW * 32) {
-        uint4 q[kV];
+  //    never of m).
+  const int nv_all = slots * (kUnitK / 8);  // 16-byte vectors per token
+  const int per = (nv_all + kW * 32 - 1) / (kW * 32);
+  if (NT == 1 && full && m <= 2 && m * per <= 4) {
+    // Few vectors per thread: they stay in registers from the load to the
+    // f16 store.  Each warp leaves its maximum per token in xmax[tok * kW +
+    // warp]; after one barrier every thread derives the shift itself.
+    constexpr int kV = 4;
+    uint4 q[kV];
+    uint32_t mx0 = 0, mx1 = 0;
 #pragma unroll
-        for (int i = 0; i < kV; ++i) {
-          const int v = v0 + i * kW * 32;
-          const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
-          const int uk = all_units ? s : (uk_begin + s) % units;
-          const int kk = uk * kUnitK + within;
-          q[i] = make_uint4(0, 0, 0, 0);
-          if (v < nv && kk < p.k) q[i] = __ldg(reinterpret_cast<const uint4 *>(xrow + kk));
-        }
-#pragma unroll
-        for (int i = 0; i < kV; ++i) {
-          const int v = v0 + i * kW * 32;
-          if (v >= nv) break;
-          mx = absmax8(mx, q[i]);
-          if (full) *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) = q[i];
-        }
+    for (int j = 0; j < kV; ++j) {
+      const int tok = j / per, v = threadIdx.x + (j - tok * per) * kW * 32;
+      q[j] = make_uint4(0, 0, 0, 0);
+      if (tok < m && v < nv_all) {
+        const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
+        const int uk = all_units ? s : (uk_begin + s) % units;
+        const int kk = uk * kUnitK + within;
+        if (kk < p.k) q[j] = __ldg(reinterpret_cast<const uint4 *>(p.x + int64_t(tok) * p.k + kk));
       }
-      mx = max(mx & 0xFFFFu, mx >> 16);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
-      if (lane == 0 && mx != 0) atomicMax(&ct.xmax[tok], mx);
     }
-  }
-  consumer_sync();
-  if (threadIdx.x < m) {
-    const uint32_t b = ct.xmax[threadIdx.x];
-    int sh = 0;
-    if (b != 0 && b < 0x7F80u) sh = 14 - ilogbf(__uint_as_float(b << 16));
-    ct.shift[threadIdx.x] = sh;
-  }
-  consumer_sync();
-  if (full) {
-    const int nv = slots * (kUnitK / 8);
-    for (int tok = 0; tok < m; ++tok) {
-      const int sh = ct.shift[tok];
-      for (int v = threadIdx.x; v < nv; v += kW * 32) {
-        uint4 *q = reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8));
-        *q = scale_to_f16(*q, sh);  // written by this same thread above
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+      if (j / per == 0) mx0 = absmax8(mx0, q[j]);
+      else mx1 = absmax8(mx1, q[j]);
+    }
+    mx0 = max(mx0 & 0xFFFFu, mx0 >> 16);
+    mx1 = max(mx1 & 0xFFFFu, mx1 >> 16);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mx0 = max(mx0, __shfl_xor_sync(0xFFFFFFFFu, mx0, o));
+      mx1 = max(mx1, __shfl_xor_sync(0xFFFFFFFFu, mx1, o));
+    }
+    if (lane == 0) {
+      ct.xmax[warp] = mx0;
+      if (m == 2) ct.xmax[kW + warp] = mx1;
+    }
+    consumer_sync();
+    int sh[2] = {0, 0};
+#pragma unroll
+    for (int tok = 0; tok < 2; ++tok) {
+      if (tok >= m) break;
+      uint32_t b = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kW; ++w2) b = max(b, ct.xmax[tok * kW + w2]);
+      if (b != 0 && b < 0x7F80u) sh[tok] = 14 - ilogbf(__uint_as_float(b << 16));
+      if (threadIdx.x == tok) ct.shift[tok] = sh[tok];
+    }
+#pragma unroll
+    for (int j = 0; j < kV; ++j) {
+      const int tok = j / per, v = threadIdx.x + (j - tok * per) * kW * 32;
+      if (tok < m && v < nv_all)
+        *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) =
+            scale_to_f16(q[j], tok == 0 ? sh[0] : sh[1]);
+    }
+    consumer_sync();
+  } else {
+    // In full mode the raw bf16 values land in shared memory on the same
+    // pass and are converted in place afterwards.
+    if (threadIdx.x < 16) ct.xmax[threadIdx.x] = 0;
+    consumer_sync();
+    {
+      const int nv = nv_all;
+      for (int tok = 0; tok < m; ++tok) {
+        const uint16_t *xrow = p.x + int64_t(tok) * p.k;
+        uint32_t mx = 0;
+        // four vectors per thread per round, every load issued before any
+        // shared-memory store (the stores go through generic pointers, which
+        // would otherwise keep each load waiting for the previous store)
+        constexpr int kV = 4;
+        for (int v0 = threadIdx.x; v0 < nv; v0 += kV * kW * 32) {
+          uint4 q[kV];
+#pragma unroll
+          for (int i = 0; i < kV; ++i) {
+            const int v = v0 + i * kW * 32;
+            const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
+            const int uk = all_units ? s : (uk_begin + s) % units;
+            const int kk = uk * kUnitK + within;
+            q[i] = make_uint4(0, 0, 0, 0);
+            if (v < nv && kk < p.k) q[i] = __ldg(reinterpret_cast<const uint4 *>(xrow + kk));
+          }
+#pragma unroll
+          for (int i = 0; i < kV; ++i) {
+            const int v = v0 + i * kW * 32;
+            if (v >= nv) break;
+            mx = absmax8(mx, q[i]);
+            if (full) *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) = q[i];
+          }
+        }
+        mx = max(mx & 0xFFFFu, mx >> 16);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+        if (lane == 0 && mx != 0) atomicMax(&ct.xmax[tok], mx);
       }
     }
     consumer_sync();
+    if (threadIdx.x < m) {
+      const uint32_t b = ct.xmax[threadIdx.x];
+      int sh = 0;
+      if (b != 0 && b < 0x7F80u) sh = 14 - ilogbf(__uint_as_float(b << 16));
+      ct.shift[threadIdx.x] = sh;
+    }
+    consumer_sync();
+    if (full) {
+      const int nv = nv_all;
+      for (int tok = 0; tok < m; ++tok) {
+        const int sh = ct.shift[tok];
+        for (int v = threadIdx.x; v < nv; v += kW * 32) {
+          uint4 *q = reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8));
+          *q = scale_to_f16(*q, sh);  // written by this same thread above
+        }
+      }
+      consumer_sync();
+    }
   }
   const float gd = __ldg(p.g_dec);
 
