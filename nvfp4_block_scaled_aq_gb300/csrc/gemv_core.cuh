@@ -256,7 +256,7 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
 }
 
 // One unit of one warp: both k-tiles, MMAs of the two tiles interleaved.
-// wlo/whi: the lane's 16 nibble bytes of rows g / g+8 per tile; sw: the
+// wlo/whi: the lane's 16 nibble bytes of fragment rows g / g+8 per tile; sw: the
 // lane's scale word per tile (rows g, g+8 x blocks 2c, 2c+1); xr: the
 // lane's 32 activations per tile and n8 block of tokens, as f16 pairs.
 template <int NT>
@@ -407,14 +407,18 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
   if (u_begin >= u_end) return;
   const int S = r.stages, m = r.m, units = p.units;
 
-  // 128-byte swizzle: logical 16-byte chunk ch of box row r sits at ch ^ (r & 7);
-  // rows rg*16 + g and rg*16 + g + 8 both have r & 7 == g.
+  // 128-byte swizzle: logical 16-byte chunk ch of box row r sits at ch ^ (r & 7).
+  // Fragment row g of the MMA holds stored row sg = sigma(g) (and sg + 8):
+  // the eight lanes of each quarter-warp then read rows sg and sg ^ 4,
+  // whose swizzled chunks fill all 32 banks once -- with sg = g the rows g
+  // and g + 1 would share banks.  The rows are relabelled in the epilogue.
+  const int sg = (g >> 1) | ((g & 1) << 2);
   int off_lo[2], off_hi[2], off_sc[2];
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
-    off_lo[t] = (rg * 16 + g) * kUnitCols + (((t * 4 + c) ^ g) << 4);
-    off_hi[t] = (rg * 16 + g + 8) * kUnitCols + (((t * 4 + c) ^ g) << 4);
-    off_sc[t] = kPackedStage + rg * (kKT * 128) + t * 128 + lane * 4;
+    off_lo[t] = (rg * 16 + sg) * kUnitCols + (((t * 4 + c) ^ sg) << 4);
+    off_hi[t] = (rg * 16 + sg + 8) * kUnitCols + (((t * 4 + c) ^ sg) << 4);
+    off_sc[t] = kPackedStage + rg * (kKT * 128) + t * 128 + (4 * sg + c) * 4;
   }
 
   // -- which k-units this CTA touches: all of them when its range covers a
@@ -624,7 +628,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
       }
     }
 
-    // -- epilogue: this warp holds rows g, g+8 x tokens nt*8 + 2c + {0,1};
+    // -- epilogue: this warp holds rows sg, sg+8 x tokens nt*8 + 2c + {0,1};
     //    the two k-tile accumulators are added in a fixed order
     const bool complete = (uk0 == 0 && uk1 == units);
     const int64_t unit0 = rb * units;
@@ -650,7 +654,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int token = nt * 8 + 2 * c + (i & 1);
-        const int row_local = rg * 16 + g + 8 * (i >> 1);
+        const int row_local = rg * 16 + sg + 8 * (i >> 1);
         const int64_t row = rb * kRB + row_local;
         const float v = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[min(token, 15)]);
         vown[nt][i] = v;
@@ -679,7 +683,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int token = nt * 8 + 2 * c + (i & 1);
-          const int row_local = rg * 16 + g + 8 * (i >> 1);
+          const int row_local = rg * 16 + sg + 8 * (i >> 1);
           const int64_t row = rb * kRB + row_local;
           if (!ok || token >= m || row >= p.n) continue;
           const int64_t at = (zrow + token) * kRB + row_local;  // word of contributor j: at + j * qs
@@ -749,7 +753,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int token = nt * 8 + 2 * c + (i & 1);
-            const int row_local = rg * 16 + g + 8 * (i >> 1);
+            const int row_local = rg * 16 + sg + 8 * (i >> 1);
             const int64_t row = rb * kRB + row_local;
             if (token >= m || row >= p.n) continue;
             const float *src = r.partial + (rb * p.max_contrib * kRB + row_local) * 16 + token;
