@@ -40,11 +40,11 @@ NOMINAL_HBM_GBS = 8000.0  # the 8 TB/s denominator the metric names
 # capture), keyed by the workload and the sha1 of the GEMV kernel sources the
 # capture was taken on; when they change the figure no longer applies (null).
 NCU_TRAFFIC = {
-    # four launches of layer 0, m = 1: 27,715,328 + 15,111,168 + 137,556,480
-    # + 67,927,552 bytes (profiles/gemv_kernel_31b_layer_dram_traffic.md);
-    # the key is of the sources after the ticket count per row block became a
-    # named host constant, the device code of gemv_kernel unchanged
-    ("gemma4-31b-shaped decode-step weight stream", 1, "c54c5cf063bcddeec599485d47d42ca4f003b1b6"): 248310528,
+    # four launches of layer 0, m = 1, captured without cache flushing so the
+    # L2 prefetch of the next projection counts where it is issued: reads
+    # 33,598,976 + 17,451,776 + 138,394,112 + 45,573,888, writes 21,870,080
+    # (profiles/gemv_kernel_31b_layer_dram_traffic.md)
+    ("gemma4-31b-shaped decode-step weight stream", 1, "2b9a53b5d6761bf7c8e1b5b51be7ff629fdccbe8"): 256888832,
 }
 
 
