@@ -63,6 +63,8 @@ def _declare(L):
     L.aqo_gemv_q.argtypes = [_p, _p, C.c_float, _p, _p, _p, _i64, _i64, _i64,
                              _p, _i64, _p]
     L.aqo_gemv_q.restype = None
+    L.aqo_gemv_bf16.argtypes = [_p, _p, _i64, _i64, _i64, _p, _i64, _p]
+    L.aqo_gemv_bf16.restype = None
     for name, tin, tout in (("aqo_bf16_round_array", np.float32, np.uint16),
                             ("aqo_e4m3_encode_array", np.float32, np.uint8),
                             ("aqo_e4m3_decode_array", np.uint8, np.float32),
@@ -210,6 +212,24 @@ def gemv(packed, scales, g_dec, x, rows=None):
     y = np.empty((m, nrows), np.float64)
     lib().aqo_gemv(pp, ps, C.c_float(g_dec), px, m, n, k, prow, nrows,
                    y.ctypes.data)
+    return y
+
+
+def gemv_bf16(W, x, rows=None):
+    """fp64 y [m, nrows] = x [m,k] times bf16 weight rows W [n,k] (both bf16 bits)."""
+    W, pw = _c(W, np.uint16)
+    x, px = _c(np.atleast_2d(x), np.uint16)
+    n, k = W.shape
+    m = x.shape[0]
+    assert x.shape[1] == k
+    if rows is None:
+        nrows, prow = n, None
+    else:
+        rows, prow = _c(rows, np.int64)
+        nrows = rows.size
+        assert rows.min(initial=0) >= 0 and rows.max(initial=0) < max(n, 1)
+    y = np.empty((m, nrows), np.float64)
+    lib().aqo_gemv_bf16(pw, px, m, n, k, prow, nrows, y.ctypes.data)
     return y
 
 

@@ -260,6 +260,22 @@ void aqo_gemv(const uint8_t *packed, const uint8_t *scales, float g_dec,
   }
 }
 
+/* [U]: the plain dot product of each selected weight row with each token,
+ * every bf16 value widened exactly and summed in fp64 in k order. */
+void aqo_gemv_bf16(const uint16_t *w, const uint16_t *x, int64_t m, int64_t n, int64_t k,
+                   const int64_t *rows, int64_t nrows, double *y) {
+  if (rows == NULL) nrows = n;
+  for (int64_t t = 0; t < m; ++t) {
+    for (int64_t i = 0; i < nrows; ++i) {
+      int64_t row = rows ? rows[i] : i;
+      double acc = 0.0;
+      for (int64_t j = 0; j < k; ++j)
+        acc += (double)aqo_bf16_to_f32(x[t * k + j]) * (double)aqo_bf16_to_f32(w[row * k + j]);
+      y[t * nrows + i] = acc;
+    }
+  }
+}
+
 /* R9: every token row is quantised like a weight tensor of one row. */
 int aqo_quantize_act(const uint16_t *x, int64_t m, int64_t k, uint8_t *packed,
                      uint8_t *scales, float *g_dec) {

@@ -27,6 +27,9 @@
  *        setting the decomposition rebuilds the original weight bit-for-bit.
  *   [W]  Weightless docs, "GPU and cache acceleration", "Future work": a
  *        GEMV that dequantises 4-bit weights in registers.
+ *   [U]  AttnQuant docs, "GPU acceleration", "Where GPU time goes": the
+ *        attention projections (when left unquantised) and the tied
+ *        lm_head / embedding are bf16 weights streamed by plain GEMVs.
  *   [F]  NVFP4 format: E2M1 element grid {0, +-0.5, +-1, +-1.5, +-2, +-3,
  *        +-4, +-6}; E4M3 (float8_e4m3fn: bias 7, max 448, no infinities)
  *        block scale per 16 elements; one fp32 per-tensor scale.  The
@@ -117,6 +120,12 @@ void aqo_gemv_q(const uint8_t *w_packed, const uint8_t *w_scales, float w_gdec,
                 const uint8_t *x_packed, const uint8_t *x_scales,
                 const float *x_gdec, int64_t m, int64_t n, int64_t k,
                 const int64_t *rows, int64_t nrows, double *y);
+
+/* [U] GEMV of a bf16 weight: y[m, i] = sum_k x[m,k] * w[rows[i],k] in
+ * fp64, k ascending, both operands bf16 [.., k] row-major.  rows / nrows
+ * as in aqo_gemv. */
+void aqo_gemv_bf16(const uint16_t *w, const uint16_t *x, int64_t m, int64_t n, int64_t k,
+                   const int64_t *rows, int64_t nrows, double *y);
 
 /* Element-wise array forms of the five scalar conversions above (one call
  * per element, in order), so tests can sweep many values cheaply. */

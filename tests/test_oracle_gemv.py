@@ -125,3 +125,47 @@ def test_gemv_q_matches_exact_rational_sum(oracle_mod):
             ex = sum(a * b for a, b in zip(xh, wh[i]))
             scale = sum(abs(a * b) for a, b in zip(xh, wh[i]))
             assert abs(Fraction(y[t, i]) - ex) <= scale * Fraction(1, 2 ** 50)
+
+
+# ------------------------------------------------------------ bf16 GEMV pins
+
+def test_gemv_bf16_matches_exact_rational_sum(oracle_mod):
+    """Brute force on a tiny problem: the exact rational sum of x * w over
+    bf16 values; the oracle's fp64 sum agrees to fp64 rounding."""
+    n, k, m = 6, 40, 3
+    W = inputs.bits_u16(inputs.weight(n, k, seed=61))
+    x = inputs.bits_u16(inputs.tokens(m, k, seed=62))
+    y = oracle_mod.gemv_bf16(W, x)
+    wf, xf = f32_of(W), f32_of(x)
+    for t in range(m):
+        for i in range(n):
+            terms = [Fraction(float(xf[t, j])) * Fraction(float(wf[i, j])) for j in range(k)]
+            ex, scale = sum(terms), sum(abs(v) for v in terms)
+            assert abs(Fraction(y[t, i]) - ex) <= scale * Fraction(1, 2 ** 50)
+
+
+def test_gemv_bf16_one_hot_and_rows(oracle_mod):
+    """A one-hot token returns the weight column exactly; `rows` selects rows."""
+    n, k = 9, 24
+    W = inputs.bits_u16(inputs.weight(n, k, seed=63))
+    wf = f32_of(W)
+    for col in (0, 7, 23):
+        x = np.zeros((1, k), np.uint16)
+        x[0, col] = bf16_of([1.0])[0]
+        assert np.array_equal(oracle_mod.gemv_bf16(W, x)[0], wf[:, col].astype(np.float64))
+    x = inputs.bits_u16(inputs.tokens(2, k, seed=64))
+    rows = np.array([8, 0, 3])
+    assert np.array_equal(oracle_mod.gemv_bf16(W, x, rows=rows), oracle_mod.gemv_bf16(W, x)[:, rows])
+
+
+def test_gemv_bf16_is_the_matrix_product_of_the_decoded_values(oracle_mod):
+    """Against numpy's fp64 matrix product of the decoded bf16 values (an
+    independent summation): equal within the fp64 rounding of two orders."""
+    n, k, m = 33, 200, 4
+    W = inputs.bits_u16(inputs.weight(n, k, seed=65))
+    x = inputs.bits_u16(inputs.tokens(m, k, seed=66))
+    ref = f32_of(x).astype(np.float64) @ f32_of(W).astype(np.float64).T
+    bound = (np.abs(f32_of(x)).astype(np.float64) @ np.abs(f32_of(W)).astype(np.float64).T) * 2e-15
+    assert np.all(np.abs(oracle_mod.gemv_bf16(W, x) - ref) <= bound)
+    # a transposed operand or a dropped term would not survive this
+    assert not np.allclose(oracle_mod.gemv_bf16(W[:, ::-1].copy(), x), ref)
