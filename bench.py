@@ -295,6 +295,42 @@ def time_region(run_step, steps, warmup, stream, dist, sampler=None):
     return dist.max(e0.elapsed_time(e1) / 1e3)
 
 
+def bf16_lm_head_leg(stream, dist, a, device):
+    """The bf16 GEMV on the ~31B tied lm_head [262144, 5376] at m = 1
+    (2.82 GB, far larger than L2): a CUDA graph of 8 PDL-chained calls,
+    event-timed on the launching stream."""
+    import torch
+    from nvfp4_block_scaled_aq_gb300 import aq, inputs
+    n, k = inputs.LM_HEAD_31B
+    W = inputs.weight(n, k, seed=inputs.seed_of(9000), device=device, outliers=False)
+    x = inputs.tokens(1, k, seed=inputs.seed_of(9001), device=device)
+    y = torch.empty((1, n), dtype=torch.bfloat16, device=device)
+    ws = torch.zeros(aq.gemv_bf16_workspace_bytes(n, k, 1), dtype=torch.uint8, device=device)
+    calls = 8
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        aq.gemv_bf16(W, x, y, ws, flags=aq.STEP_PDL, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(calls):
+                aq.gemv_bf16(W, x, y, ws, flags=aq.STEP_PDL, stream=stream)
+    torch.cuda.synchronize()
+
+    def run():
+        with torch.cuda.stream(stream):
+            g.replay()
+    reps = max(3, a.steps // 10)
+    secs = time_region(run, reps, a.warmup, stream, dist) / (reps * calls)
+    torch.cuda.synchronize()
+    del g
+    byts = 2 * n * k + 2 * k + 2 * n
+    peak, _ = load_peaks()
+    return {"shape": [n, k], "m": 1, "us_per_call": round(secs * 1e6, 2),
+            "GBps": round(byts / secs / 1e9, 1), "frac_of_peak": round(byts / secs / 1e9 / peak, 4),
+            "kernel": "gemv_bf16_kernel<1>, 8 PDL-chained calls per CUDA graph"}
+
+
 def kernel_sha():
     h = hashlib.sha1()
     for name in ("gemv_core.cuh", "gemv.cu"):
@@ -431,6 +467,8 @@ def run_aq(a, dist):
                "path": "aq_decode_step_weights graph replay, pinned host buffers copied "
                        "in and out inside the timed region"}
     del g_pdl
+    if not a.no_extras and a.workload == "31b":
+        extras["bf16_lm_head"] = bf16_lm_head_leg(stream, dist, a, device)
 
     st = aq.poll_device_status()
     if st != aq.OK:

@@ -260,6 +260,32 @@ AQ_API aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj
                                  int32_t m, uint32_t flags, void *workspace,
                                  size_t workspace_bytes, aq_stream_t stream);
 
+/* GEMV of a weight kept in bf16: the projections the method leaves
+ * unquantised -- the tied lm_head / embedding, and the attention projections
+ * when they are excluded from quantisation (AttnQuant docs, "GPU
+ * acceleration", "Where GPU time goes": these bf16 families stream beside
+ * the NVFP4 MLP in every decode step; "NVFP4 quantization": 2.82 GB of bf16
+ * embedding / lm_head on the 31B model).
+ *
+ * y[t, i] = bf16( sum_k x[t, k] * w[i, k] ), fp32 accumulation.  w [n, k]
+ * bf16 row-major (device, caller-owned, read only), 1 <= n <= 2^24,
+ * 8 <= k <= 2^20 with k % 8 == 0; x [m, k] and y [m, n] bf16 row-major,
+ * 1 <= m <= AQ_MAX_M; w, x, y 16-byte aligned, y not overlapping x or w.
+ * The split over K is fixed by (n, k) and the device, so the result does
+ * not depend on timing, and each token's output equals the m = 1 call bit
+ * for bit.  flags: 0 or AQ_STEP_PDL (the kernel waits for the previous
+ * launch on the stream programmatically, after it has started fetching
+ * weights).  workspace: aq_gemv_bf16_workspace_bytes(n, k, m) bytes of
+ * device memory, 256-byte aligned, zero-filled once, with the same
+ * contract as the NVFP4 GEMV's (and interchangeable with it: one workspace
+ * of the larger size serves both).  Errors: AQ_ERR_SHAPE, AQ_ERR_ALIGNMENT,
+ * AQ_ERR_INVALID_ARG, AQ_ERR_WORKSPACE before any launch; AQ_ERR_TIMEOUT
+ * through aq_poll_device_status. */
+AQ_API size_t aq_gemv_bf16_workspace_bytes(int32_t n, int32_t k, int32_t m);
+AQ_API aq_status aq_gemv_bf16(const uint16_t *w, int32_t n, int32_t k, const uint16_t *x,
+                              int32_t m, uint16_t *y, uint32_t flags, void *workspace,
+                              size_t workspace_bytes, aq_stream_t stream);
+
 /* The decode step's weight stream as ONE persistent kernel ("GPU
  * acceleration", "CUDA graph capture": replay the step without per-kernel
  * dispatch; "Q/K/V fusion": one weight read per fused projection).

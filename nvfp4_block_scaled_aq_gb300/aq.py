@@ -87,6 +87,8 @@ def _declare(L):
         "aq_gemv_workspace_bytes": ([_i32, _i32, _i32], _sz),
         "aq_gemv_nvfp4": ([W, _p, _i32, _p, C.c_int, _p, _sz, _p], C.c_int),
         "aq_gemv_nvfp4_noalloc": ([W, _p, _i32, _p, C.c_int, _p], C.c_int),
+        "aq_gemv_bf16_workspace_bytes": ([_i32, _i32, _i32], _sz),
+        "aq_gemv_bf16": ([_p, _i32, _i32, _p, _i32, _p, C.c_uint32, _p, _sz, _p], C.c_int),
         "aq_quantize_act_nvfp4": ([_p, _i32, _i32, _p, _p, _p, _p], C.c_int),
         "aq_decode_step_weights": ([W, _i32, C.POINTER(_p), C.POINTER(_p), _i32,
                                     C.c_uint32, _p, _sz, _p], C.c_int),
@@ -206,6 +208,21 @@ def gemv(w: Nvfp4Weight, x, y, workspace, path=PATH_AUTO, stream=None):
     check(lib().aq_gemv_nvfp4(C.byref(wc), _ptr(x), m, _ptr(y), path, _ptr(workspace),
                               workspace.numel() * workspace.element_size(),
                               _stream(stream)))
+
+
+def gemv_bf16_workspace_bytes(n, k, m=1):
+    b = int(lib().aq_gemv_bf16_workspace_bytes(n, k, m))
+    if b == 0:
+        raise AqError(ERR_SHAPE, last_error() or "bad bf16 GEMV shape")
+    return b
+
+
+def gemv_bf16(W, x, y, workspace, flags=0, stream=None):
+    """y [m, n] = x [m, k] W [n, k]^T for a bf16 weight (aq_gemv_bf16)."""
+    n, k = W.shape
+    check(lib().aq_gemv_bf16(_ptr(W), n, k, _ptr(x), x.shape[0], _ptr(y), flags,
+                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _stream(stream)))
 
 
 def quantize_act(x, packed, scales, g_dec, stream=None):

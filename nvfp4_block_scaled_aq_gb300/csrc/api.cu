@@ -296,6 +296,43 @@ aq_status aq_gemv_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m, 
   return launched(launch_gemv(*w, x, m, y, workspace, false, *dev, st), what);
 }
 
+// bf16 weight shape: rows of whole 16-byte vectors.
+static aq_status check_bf16_nk(int32_t n, int32_t k) {
+  if (n < 1 || n > kMaxN)
+    return set_error(AQ_ERR_SHAPE, "n = %d outside [1, %d]", n, kMaxN);
+  if (k < 8 || k > kMaxK || k % 8 != 0)
+    return set_error(AQ_ERR_SHAPE, "k = %d must be a multiple of 8 in [8, %d]", k, kMaxK);
+  return AQ_OK;
+}
+
+size_t aq_gemv_bf16_workspace_bytes(int32_t n, int32_t k, int32_t m) {
+  if (check_bf16_nk(n, k) != AQ_OK || m < 1 || m > AQ_MAX_M) return 0;
+  const DeviceInfo *dev = device_info();
+  if (!dev) return 0;
+  return gemv_bf16_workspace_bytes(n, k, *dev);
+}
+
+aq_status aq_gemv_bf16(const uint16_t *w, int32_t n, int32_t k, const uint16_t *x, int32_t m,
+                       uint16_t *y, uint32_t flags, void *workspace, size_t workspace_bytes,
+                       aq_stream_t stream) {
+  const char *what = "aq_gemv_bf16";
+  aq_status s = check_bf16_nk(n, k);
+  if (s != AQ_OK) return s;
+  if (m < 1 || m > AQ_MAX_M)
+    return set_error(AQ_ERR_SHAPE, "%s: m = %d outside [1, %d]", what, m, AQ_MAX_M);
+  if (flags & ~AQ_STEP_PDL) return set_error(AQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", what, flags);
+  if (!w || !x || !y) return set_error(AQ_ERR_INVALID_ARG, "%s: w, x and y must not be NULL", what);
+  if (!aligned(w, 16) || !aligned(x, 16) || !aligned(y, 16))
+    return set_error(AQ_ERR_ALIGNMENT, "%s: w, x and y must be 16-byte aligned", what);
+  const DeviceInfo *dev = device_info();
+  if (!dev) return AQ_ERR_UNSUPPORTED;
+  if ((s = check_ws(workspace, workspace_bytes, gemv_bf16_workspace_bytes(n, k, *dev), what)) != AQ_OK)
+    return s;
+  return launched(launch_gemv_bf16(w, n, k, x, m, y, workspace, (flags & AQ_STEP_PDL) != 0, *dev,
+                                   reinterpret_cast<cudaStream_t>(stream)),
+                  what);
+}
+
 aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,
                                  const uint16_t *const *x, uint16_t *const *y, int32_t m,
                                  uint32_t flags, void *workspace, size_t workspace_bytes,

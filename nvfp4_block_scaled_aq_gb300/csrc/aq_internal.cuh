@@ -231,6 +231,12 @@ cudaError_t launch_mma(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint1
 // boxes of 16 B x n_box rows (gemv.cu).
 bool encode_act_maps(const uint8_t *xq, const uint8_t *xs, int m, int k, int scale_pitch,
                      int n_box, CUtensorMap *tm_x, CUtensorMap *tm_xs);
+// The bf16 GEMV (gemv_bf16.cu): plan, workspace and launch.
+GemvPlan plan_gemv_bf16(int n, int k, const DeviceInfo &dev);
+size_t gemv_bf16_workspace_bytes(int n, int k, const DeviceInfo &dev);
+cudaError_t launch_gemv_bf16(const uint16_t *w, int n, int k, const uint16_t *x, int m,
+                             uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
+                             cudaStream_t st);
 // Register-decode kernel only (gemv.cu).
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,

@@ -200,6 +200,13 @@ bool encode_maps(const aq_nvfp4_weight &w, CUtensorMap *tm_w, CUtensorMap *tm_s)
                     false);
 }
 
+// bf16 weight [n, k] as a byte matrix [n rows, 2k bytes]: boxes of 128 B x
+// 128 rows with the 128-byte swizzle, exactly like the NVFP4 nibble boxes.
+bool encode_bf16_map(const uint16_t *w, int n, int k, CUtensorMap *tm) {
+  if (!encoder()) return false;
+  return cached_map(tm, w, uint64_t(k) * 2, uint64_t(n), kUnitCols, kRB, true);
+}
+
 }  // namespace core
 
 bool encode_act_maps(const uint8_t *xq, const uint8_t *xs, int m, int k, int scale_pitch,
@@ -290,6 +297,7 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   p.max_contrib = plan.max_contrib;
   p.grid = plan.grid;
   p.direct = direct_partials_fit(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
+  p.scale_box = 1;
   p.nx_w = p.nx_s = nullptr;
   p.nx_total = 0;
   p.nx_units = p.nx_grid = p.nx_pf = 0;
@@ -365,6 +373,7 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   p.max_contrib = plan.max_contrib;
   p.grid = plan.grid;
   p.direct = direct_partials_fit(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
+  p.scale_box = 1;
   p.nx_w = p.nx_s = nullptr;  // no prefetch of a next projection
   p.nx_total = 0;
   p.nx_units = p.nx_grid = p.nx_pf = 0;

@@ -103,6 +103,8 @@ struct Proj {
   int nx_pf;                // units per CTA to prefetch
   int direct;               // split-K partials go to the zero region, see
                             // direct_partials_fit()
+  int scale_box;            // 1: each unit also loads its scale box (NVFP4);
+                            // 0: the unit is the 16 KiB weight box only (bf16)
 };
 
 // The reducer of a split row block can poll the partials themselves when
@@ -326,9 +328,10 @@ __device__ __forceinline__ bool produce(const Proj &p, uint8_t *base, Ctrl &ct, 
     const int64_t rb = u / p.units;
     const int uk = int(u - rb * p.units);
     uint8_t *stage = base + st * kStageBytes;
-    mbar_expect_tx(&ct.full[st], kStageBytes);
+    mbar_expect_tx(&ct.full[st], p.scale_box ? kStageBytes : kPackedStage);
     tma_load_2d(stage, p.tm_w, uk * kUnitCols, int(rb * kRB), &ct.full[st]);
-    tma_load_2d(stage + kPackedStage, p.tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[st]);
+    if (p.scale_box)
+      tma_load_2d(stage + kPackedStage, p.tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[st]);
   }
   return true;
 }
@@ -390,6 +393,158 @@ __device__ __forceinline__ void prefetch_x_l2(const Proj &p, int m) {
       asm volatile("prefetch.global.L2 [%0];" ::"l"(p.x + int64_t(tok) * p.k + kk));
   }
 }
+
+// The end of one row block's share of a CTA for one warp: vown[nt][i] is
+// the warp's fp32 sum (before g_dec) for fragment rows sg, sg + 8 (i >> 1)
+// and tokens nt*8 + 2c + (i & 1).  A row block wholly inside the CTA's range
+// is written as bf16(g_dec * v).  Split row blocks: contributor 0 (the CTA
+// whose range ends in this row block, so usually among the last to finish
+// it) reduces, keeping its own partial in registers and adding the others'
+// in contributor order; no barrier spans the warps, and no other
+// contributor waits.
+template <int NT>
+__device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t rb, bool complete,
+                                            const float (&vown)[NT][4], float gd, int rg, int sg,
+                                            int lane, volatile int *aborted) {
+  const int units = p.units, m = r.m, c = lane & 3;
+  const int64_t grid = p.grid;
+  const int64_t unit0 = rb * units;
+  const int64_t own_lo = owner_of(unit0, p.total, grid);
+  const int contrib = int(owner_of(unit0 + units - 1, p.total, grid) - own_lo + 1);
+  const int jj = int(blockIdx.x - own_lo);
+  //  * direct: the others store ~bits(partial) to the zero region and
+  //    leave; the reducer polls those words (bounded) until none is zero,
+  //    then puts the zeros back.
+  //  * otherwise: the others store plain partials and publish them with
+  //    one release-add per (row block, row group); the reducer waits
+  //    (bounded) for the count, reads the partials and clears the count.
+  const bool reducer = !complete && jj == 0;
+  const bool direct = NT == 1 && p.direct;
+  const int64_t zrow = (rb * (p.max_contrib - 1) - 1) * m;  // + (j * m + token) * kRB + row
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int token = nt * 8 + 2 * c + (i & 1);
+      const int row_local = rg * 16 + sg + 8 * (i >> 1);
+      const int64_t row = rb * kRB + row_local;
+      const float v = vown[nt][i];
+      if (token >= m || row >= p.n) continue;
+      if (complete) {
+        p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(v, gd));
+      } else if (!reducer) {
+        if (direct)
+          asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(
+                           r.zero + (zrow + int64_t(jj) * m + token) * kRB + row_local),
+                       "r"(~__float_as_uint(v))
+                       : "memory");
+        else
+          r.partial[((rb * p.max_contrib + jj) * kRB + row_local) * 16 + token] = v;
+      }
+    }
+  if (!complete && !reducer && !direct) {
+    __syncwarp();  // the warp's partial stores precede lane 0's release
+    if (lane == 0)
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(r.tickets + rb * kRG + rg)
+                   : "memory");
+  } else if (reducer && direct) {
+    bool ok = true;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int token = nt * 8 + 2 * c + (i & 1);
+        const int row_local = rg * 16 + sg + 8 * (i >> 1);
+        const int64_t row = rb * kRB + row_local;
+        if (!ok || token >= m || row >= p.n) continue;
+        const int64_t at = (zrow + token) * kRB + row_local;  // word of contributor j: at + j * qs
+        const int64_t qs = int64_t(m) * kRB;
+        uint32_t w[16];
+#pragma unroll
+        for (int q = 1; q < 16; ++q) {
+          w[q] = 1u;
+          if (q < contrib)
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w[q]) : "l"(r.zero + (at + q * qs)) : "memory");
+        }
+        for (unsigned it = 0;; ++it) {
+          bool all = true;
+#pragma unroll
+          for (int q = 1; q < 16; ++q) all = all && w[q] != 0u;
+          if (all) break;
+          if (it >= kSpinLimit || *aborted) {
+            ok = false;
+            break;
+          }
+          __nanosleep(32);
+#pragma unroll
+          for (int q = 1; q < 16; ++q)
+            if (q < contrib && w[q] == 0u)
+              asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w[q]) : "l"(r.zero + (at + q * qs)) : "memory");
+        }
+        if (!ok) continue;
+        float s = __fadd_rn(0.0f, vown[nt][i]);
+#pragma unroll
+        for (int q = 1; q < 16; ++q)
+          if (q < contrib) {
+            s = __fadd_rn(s, __uint_as_float(~w[q]));
+            asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(r.zero + (at + q * qs)), "r"(0u) : "memory");
+          }
+        p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(s, gd));
+      }
+    if (!ok && !*aborted) {
+      *aborted = 1;
+      raise_status(r.status, kDevTimeout);
+    }
+  } else if (reducer) {
+    uint32_t *flag = r.tickets + rb * kRG + rg;
+    bool ok = true;
+    if (lane == 0) {
+      const unsigned want = unsigned(contrib - 1);
+      unsigned seen = 0;
+      for (unsigned it = 0;; ++it) {
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(flag) : "memory");
+        if (seen >= want) break;
+        if (it >= kSpinLimit || *aborted) {
+          ok = false;
+          break;
+        }
+        __nanosleep(32);
+      }
+      if (!ok && !*aborted) {
+        *aborted = 1;
+        raise_status(r.status, kDevTimeout);
+      }
+    }
+    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    __syncwarp();  // every lane's loads below follow lane 0's acquire
+    if (ok) {
+      const int64_t qs = int64_t(kRB) * 16;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int token = nt * 8 + 2 * c + (i & 1);
+          const int row_local = rg * 16 + sg + 8 * (i >> 1);
+          const int64_t row = rb * kRB + row_local;
+          if (token >= m || row >= p.n) continue;
+          const float *src = r.partial + (rb * p.max_contrib * kRB + row_local) * 16 + token;
+          float s = __fadd_rn(0.0f, vown[nt][i]);
+          if (contrib <= 16) {
+            float v[16];
+#pragma unroll
+            for (int q = 1; q < 16; ++q) v[q] = q < contrib ? __ldcg(src + q * qs) : 0.0f;
+#pragma unroll
+            for (int q = 1; q < 16; ++q)
+              if (q < contrib) s = __fadd_rn(s, v[q]);
+          } else {
+            for (int q = 1; q < contrib; ++q) s = __fadd_rn(s, __ldcg(src + q * qs));
+          }
+          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(s, gd));
+        }
+      __syncwarp();
+      if (lane == 0) *flag = 0;
+    }
+  }}
 
 // Consumers: the whole of this CTA's share of projection p -- activation
 // staging, the unit loop, and the split-K epilogue.  Called by the kW
@@ -631,149 +786,15 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
     // -- epilogue: this warp holds rows sg, sg+8 x tokens nt*8 + 2c + {0,1};
     //    the two k-tile accumulators are added in a fixed order
     const bool complete = (uk0 == 0 && uk1 == units);
-    const int64_t unit0 = rb * units;
-    const int64_t own_lo = owner_of(unit0, p.total, grid);
-    const int contrib = int(owner_of(unit0 + units - 1, p.total, grid) - own_lo + 1);
-    const int jj = int(blockIdx.x - own_lo);
-    // Split row blocks: contributor 0 (the CTA whose range ends in this row
-    // block, so usually among the last to finish it) reduces, keeping its
-    // own partial in registers and adding the others' in contributor order;
-    // no barrier spans the warps, and no other contributor waits.
-    //  * direct: the others store ~bits(partial) to the zero region and
-    //    leave; the reducer polls those words (bounded) until none is zero,
-    //    then puts the zeros back.
-    //  * otherwise: the others store plain partials and publish them with
-    //    one release-add per (row block, row group); the reducer waits
-    //    (bounded) for the count, reads the partials and clears the count.
-    const bool reducer = !complete && jj == 0;
-    const bool direct = NT == 1 && p.direct;
-    float vown[NT][4];
-    const int64_t zrow = (rb * (p.max_contrib - 1) - 1) * m;  // + (j * m + token) * kRB + row
+    float v[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const int token = nt * 8 + 2 * c + (i & 1);
-        const int row_local = rg * 16 + sg + 8 * (i >> 1);
-        const int64_t row = rb * kRB + row_local;
-        const float v = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[min(token, 15)]);
-        vown[nt][i] = v;
-        if (token >= m || row >= p.n) continue;
-        if (complete) {
-          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(v, gd));
-        } else if (!reducer) {
-          if (direct)
-            asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(
-                             r.zero + (zrow + int64_t(jj) * m + token) * kRB + row_local),
-                         "r"(~__float_as_uint(v))
-                         : "memory");
-          else
-            r.partial[((rb * p.max_contrib + jj) * kRB + row_local) * 16 + token] = v;
-        }
+        v[nt][i] = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[min(token, 15)]);
       }
-    if (!complete && !reducer && !direct) {
-      __syncwarp();  // the warp's partial stores precede lane 0's release
-      if (lane == 0)
-        asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(r.tickets + rb * kRG + rg)
-                     : "memory");
-    } else if (reducer && direct) {
-      bool ok = true;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int token = nt * 8 + 2 * c + (i & 1);
-          const int row_local = rg * 16 + sg + 8 * (i >> 1);
-          const int64_t row = rb * kRB + row_local;
-          if (!ok || token >= m || row >= p.n) continue;
-          const int64_t at = (zrow + token) * kRB + row_local;  // word of contributor j: at + j * qs
-          const int64_t qs = int64_t(m) * kRB;
-          uint32_t w[16];
-#pragma unroll
-          for (int q = 1; q < 16; ++q) {
-            w[q] = 1u;
-            if (q < contrib)
-              asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w[q]) : "l"(r.zero + (at + q * qs)) : "memory");
-          }
-          for (unsigned it = 0;; ++it) {
-            bool all = true;
-#pragma unroll
-            for (int q = 1; q < 16; ++q) all = all && w[q] != 0u;
-            if (all) break;
-            if (it >= kSpinLimit || *aborted) {
-              ok = false;
-              break;
-            }
-            __nanosleep(32);
-#pragma unroll
-            for (int q = 1; q < 16; ++q)
-              if (q < contrib && w[q] == 0u)
-                asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w[q]) : "l"(r.zero + (at + q * qs)) : "memory");
-          }
-          if (!ok) continue;
-          float s = __fadd_rn(0.0f, vown[nt][i]);
-#pragma unroll
-          for (int q = 1; q < 16; ++q)
-            if (q < contrib) {
-              s = __fadd_rn(s, __uint_as_float(~w[q]));
-              asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(r.zero + (at + q * qs)), "r"(0u) : "memory");
-            }
-          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(s, gd));
-        }
-      if (!ok && !*aborted) {
-        *aborted = 1;
-        raise_status(r.status, kDevTimeout);
-      }
-    } else if (reducer) {
-      uint32_t *flag = r.tickets + rb * kRG + rg;
-      bool ok = true;
-      if (lane == 0) {
-        const unsigned want = unsigned(contrib - 1);
-        unsigned seen = 0;
-        for (unsigned it = 0;; ++it) {
-          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(flag) : "memory");
-          if (seen >= want) break;
-          if (it >= kSpinLimit || *aborted) {
-            ok = false;
-            break;
-          }
-          __nanosleep(32);
-        }
-        if (!ok && !*aborted) {
-          *aborted = 1;
-          raise_status(r.status, kDevTimeout);
-        }
-      }
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      __syncwarp();  // every lane's loads below follow lane 0's acquire
-      if (ok) {
-        const int64_t qs = int64_t(kRB) * 16;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int token = nt * 8 + 2 * c + (i & 1);
-            const int row_local = rg * 16 + sg + 8 * (i >> 1);
-            const int64_t row = rb * kRB + row_local;
-            if (token >= m || row >= p.n) continue;
-            const float *src = r.partial + (rb * p.max_contrib * kRB + row_local) * 16 + token;
-            float s = __fadd_rn(0.0f, vown[nt][i]);
-            if (contrib <= 16) {
-              float v[16];
-#pragma unroll
-              for (int q = 1; q < 16; ++q) v[q] = q < contrib ? __ldcg(src + q * qs) : 0.0f;
-#pragma unroll
-              for (int q = 1; q < 16; ++q)
-                if (q < contrib) s = __fadd_rn(s, v[q]);
-            } else {
-              for (int q = 1; q < contrib; ++q) s = __fadd_rn(s, __ldcg(src + q * qs));
-            }
-            p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(s, gd));
-          }
-        __syncwarp();
-        if (lane == 0) *flag = 0;
-      }
-    }
+    finish_rows<NT>(p, r, rb, complete, v, gd, rg, sg, lane, aborted);
     u += uk1 - uk0;
   }
 }
@@ -807,6 +828,7 @@ __device__ __forceinline__ void init_ring(Ctrl &ct, int S) {
 size_t smem_bytes(int stages, int x_cap_halves);
 int stages_for(int x_cap_halves);
 bool encode_maps(const aq_nvfp4_weight &w, CUtensorMap *tm_w, CUtensorMap *tm_s);
+bool encode_bf16_map(const uint16_t *w, int n, int k, CUtensorMap *tm);
 
 }  // namespace core
 }  // namespace aq

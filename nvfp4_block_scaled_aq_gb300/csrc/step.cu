@@ -102,6 +102,7 @@ __device__ __forceinline__ Proj to_proj(const StepProj &s) {
   p.max_contrib = s.max_contrib;
   p.grid = s.grid;
   p.direct = s.direct;
+  p.scale_box = 1;
   p.nx_w = p.nx_s = nullptr;
   p.nx_total = 0;
   p.nx_units = p.nx_grid = p.nx_pf = 0;

@@ -87,6 +87,9 @@ def theta(n: int, k: int, r: int, seed: int, device="cpu",
 # gate+up, down.  The 1B-shaped stack has 26 layers, the 31B-shaped 60.
 LAYER_1B = ((1536, 1152), (1152, 1024), (13824, 1152), (1152, 6912))
 LAYER_31B = ((8192, 5376), (5376, 4096), (43008, 5376), (5376, 21504))
+# bf16 tied lm_head / embedding [vocab, hidden] of the ~31B and ~1B shapes
+LM_HEAD_31B = (262144, 5376)
+LM_HEAD_1B = (262144, 1152)
 LAYERS_1B = 26
 LAYERS_31B = 60
 PROJ_NAMES = ("qkv", "o_proj", "gate_up", "down")

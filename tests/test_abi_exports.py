@@ -100,6 +100,19 @@ def test_host_validation_without_a_device(aq):
         aq.ERR_INVALID_ARG
     assert L.aq_decode_step_weights(None, 0, None, None, 1, 0, None, 0, None) == aq.OK
     assert L.aq_quantize_nvfp4(None, 16, 64, None, None, 0, None) == aq.ERR_INVALID_ARG
+    # bf16 GEMV: k a multiple of 8, 1 <= m <= AQ_MAX_M, known flags, 16-byte
+    # aligned non-NULL buffers -- all checked before any device query
+    p16 = C.c_void_p(256)
+    assert L.aq_gemv_bf16(p16, 16, 12, p16, 1, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert L.aq_gemv_bf16(p16, 0, 64, p16, 1, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert L.aq_gemv_bf16(p16, 16, 64, p16, 0, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert L.aq_gemv_bf16(p16, 16, 64, p16, 17, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert L.aq_gemv_bf16(p16, 16, 64, p16, 1, p16, 2, None, 0, None) == aq.ERR_INVALID_ARG
+    assert L.aq_gemv_bf16(None, 16, 64, p16, 1, p16, 0, None, 0, None) == aq.ERR_INVALID_ARG
+    assert L.aq_gemv_bf16(C.c_void_p(8), 16, 64, p16, 1, p16, 0, None, 0, None) == \
+        aq.ERR_ALIGNMENT
+    assert L.aq_gemv_bf16_workspace_bytes(16, 12, 1) == 0
+    assert L.aq_gemv_bf16_workspace_bytes(16, 64, 17) == 0
 
 
 def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
