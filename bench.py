@@ -67,6 +67,8 @@ def parse():
     p.add_argument("--kernel", choices=("regdecode", "tcgen05"), default="regdecode",
                    help="GEMV kernel of the timed step (regdecode: the library's default "
                         "for m <= 16; the other one is timed among the extras)")
+    p.add_argument("--bf16-lm-head", action="store_true",
+                   help="time only the bf16 GEMV on the ~31B tied lm_head [262144, 5376], m = 1")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the eager / no-PDL / end-to-end / CPU-baseline legs")
     return p.parse_args()
@@ -527,6 +529,23 @@ def run_aq(a, dist):
 SWEEP_M = (1, 2, 4, 8, 16, 32, 64)
 
 
+def run_bf16_lm_head(a, dist):
+    """One JSON line for the bf16 GEMV leg alone (its own configuration, not
+    the headline)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(dist.local)
+    device = torch.device("cuda", dist.local)
+    stream = torch.cuda.Stream(device)
+    r = bf16_lm_head_leg(stream, dist, a, device)
+    if dist.rank == 0:
+        print(json.dumps({"metric": "bf16 GEMV HBM GB/s", "value": r["GBps"], "unit": "GB/s",
+                          "n_gpus": dist.world, "higher_is_better": True,
+                          "data": "synthetic (seeded N(0,0.02^2) weight, N(0,1) token)",
+                          "config": {"workload": "~31B tied lm_head, bf16", **r}}), flush=True)
+
+
 def run_sweep(a, dist):
     """GEMV kernels vs the block-scaled MMA path on the ~31B-shaped fused
     gate+up [43008, 5376] and down [5376, 21504] weights.  Each timing is a
@@ -675,6 +694,8 @@ def main():
             run_reference(a, dist)
         elif a.batch_sweep:
             run_sweep(a, dist)
+        elif a.bf16_lm_head:
+            run_bf16_lm_head(a, dist)
         else:
             run_aq(a, dist)
     finally:
