@@ -65,6 +65,9 @@ def _declare(L):
     L.aqo_gemv_q.restype = None
     L.aqo_gemv_bf16.argtypes = [_p, _p, _i64, _i64, _i64, _p, _i64, _p]
     L.aqo_gemv_bf16.restype = None
+    L.aqo_gemv_lowrank.argtypes = [_p, _p, C.c_float, _p, _p, _p, _i64, _p, _i64, _i64, _i64,
+                                   _p, _i64, _p]
+    L.aqo_gemv_lowrank.restype = None
     for name, tin, tout in (("aqo_bf16_round_array", np.float32, np.uint16),
                             ("aqo_e4m3_encode_array", np.float32, np.uint8),
                             ("aqo_e4m3_decode_array", np.uint8, np.float32),
@@ -230,6 +233,31 @@ def gemv_bf16(W, x, rows=None):
         assert rows.min(initial=0) >= 0 and rows.max(initial=0) < max(n, 1)
     y = np.empty((m, nrows), np.float64)
     lib().aqo_gemv_bf16(pw, px, m, n, k, prow, nrows, y.ctypes.data)
+    return y
+
+
+def gemv_lowrank(packed, scales, g_dec, s, U, V, x, rows=None):
+    """fp64 y [m, nrows] = s * (x w0_hat^T) + (x V) U^T for a quantised W0
+    (packed, canonical scales, g_dec), s fp32 [n], U bits [n,r], V bits [k,r]."""
+    packed, pp = _c(packed, np.uint8)
+    scales, ps = _c(scales, np.uint8)
+    s, pscale = _c(s, np.float32)
+    x, px = _c(np.atleast_2d(x), np.uint16)
+    n = packed.shape[0]
+    m, k = x.shape
+    r = 0 if U is None or np.asarray(U).size == 0 else np.asarray(U).size // n
+    U, pu = _c(np.asarray(U if r else np.zeros((n, 1))).reshape(n, max(r, 1)), np.uint16)
+    V, pv = _c(np.asarray(V if r else np.zeros((k, 1))).reshape(k, max(r, 1)), np.uint16)
+    assert packed.shape == (n, k // 2) and scales.shape == (n, k // 16) and s.shape == (n,)
+    if rows is None:
+        nrows, prow = n, None
+    else:
+        rows, prow = _c(rows, np.int64)
+        nrows = rows.size
+        assert rows.min(initial=0) >= 0 and rows.max(initial=0) < max(n, 1)
+    y = np.empty((m, nrows), np.float64)
+    lib().aqo_gemv_lowrank(pp, ps, C.c_float(g_dec), pscale, pu if r else None,
+                           pv if r else None, r, px, m, n, k, prow, nrows, y.ctypes.data)
     return y
 
 

@@ -276,6 +276,32 @@ void aqo_gemv_bf16(const uint16_t *w, const uint16_t *x, int64_t m, int64_t n, i
   }
 }
 
+/* [L]: the block product scaled per row, plus the rank-r term through the
+ * r projections V^T x, each a plain fp64 sum. */
+void aqo_gemv_lowrank(const uint8_t *packed, const uint8_t *scales, float g_dec, const float *s,
+                      const uint16_t *U, const uint16_t *V, int64_t r, const uint16_t *x,
+                      int64_t m, int64_t n, int64_t k, const int64_t *rows, int64_t nrows,
+                      double *y) {
+  if (rows == NULL) nrows = n;
+  for (int64_t t = 0; t < m; ++t) {
+    const uint16_t *xt = x + t * k;
+    for (int64_t i = 0; i < nrows; ++i) {
+      int64_t row = rows ? rows[i] : i;
+      double base = 0.0;
+      for (int64_t j = 0; j < k; ++j)
+        base += (double)aqo_bf16_to_f32(xt[j]) * w_hat(packed, scales, (double)g_dec, row, j, k);
+      double delta = 0.0;
+      for (int64_t q = 0; q < r; ++q) {
+        double vx = 0.0;
+        for (int64_t j = 0; j < k; ++j)
+          vx += (double)aqo_bf16_to_f32(V[j * r + q]) * (double)aqo_bf16_to_f32(xt[j]);
+        delta += (double)aqo_bf16_to_f32(U[row * r + q]) * vx;
+      }
+      y[t * nrows + i] = (double)s[row] * base + delta;
+    }
+  }
+}
+
 /* R9: every token row is quantised like a weight tensor of one row. */
 int aqo_quantize_act(const uint16_t *x, int64_t m, int64_t k, uint8_t *packed,
                      uint8_t *scales, float *g_dec) {

@@ -27,6 +27,11 @@
  *        setting the decomposition rebuilds the original weight bit-for-bit.
  *   [W]  Weightless docs, "GPU and cache acceleration", "Future work": a
  *        GEMV that dequantises 4-bit weights in registers.
+ *   [L]  AttnQuant docs, "Throughput", "The runtime reconstruction path does
+ *        not reach dense parity", and "GPU acceleration", "How the pieces
+ *        fit" (the custom op that fuses the shared-block dot product and the
+ *        low-rank delta): the runtime path evaluates s*(W0 x) + U (V^T x)
+ *        instead of a rebuilt weight.
  *   [U]  AttnQuant docs, "GPU acceleration", "Where GPU time goes": the
  *        attention projections (when left unquantised) and the tied
  *        lm_head / embedding are bf16 weights streamed by plain GEMVs.
@@ -126,6 +131,17 @@ void aqo_gemv_q(const uint8_t *w_packed, const uint8_t *w_scales, float w_gdec,
  * as in aqo_gemv. */
 void aqo_gemv_bf16(const uint16_t *w, const uint16_t *x, int64_t m, int64_t n, int64_t k,
                    const int64_t *rows, int64_t nrows, double *y);
+
+/* [L] [H] runtime low-rank GEMV with a quantised shared block:
+ * y[m, i] = s[i] * sum_k x[m,k] * w0_hat[i,k]
+ *         + sum_r U[i,r] * (sum_k V[k,r] * x[m,k]),
+ * every sum in fp64 in index order, w0_hat = e2m1(q) * sd * g_dec of the
+ * quantised W0 (packed, canonical scales); s fp32 [n], U bf16 [n, r],
+ * V bf16 [k, r], x bf16 [m, k]; r may be 0.  rows / nrows as in aqo_gemv. */
+void aqo_gemv_lowrank(const uint8_t *packed, const uint8_t *scales, float g_dec, const float *s,
+                      const uint16_t *U, const uint16_t *V, int64_t r, const uint16_t *x,
+                      int64_t m, int64_t n, int64_t k, const int64_t *rows, int64_t nrows,
+                      double *y);
 
 /* Element-wise array forms of the five scalar conversions above (one call
  * per element, in order), so tests can sweep many values cheaply. */

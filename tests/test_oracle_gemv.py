@@ -169,3 +169,65 @@ def test_gemv_bf16_is_the_matrix_product_of_the_decoded_values(oracle_mod):
     assert np.all(np.abs(oracle_mod.gemv_bf16(W, x) - ref) <= bound)
     # a transposed operand or a dropped term would not survive this
     assert not np.allclose(oracle_mod.gemv_bf16(W[:, ::-1].copy(), x), ref)
+
+
+# ------------------------------------------------------- runtime low-rank pins
+
+def lowrank_case(n, k, r, seed):
+    W0 = inputs.bits_u16(inputs.weight(n, k, seed=seed))
+    g = np.random.default_rng(seed)
+    s = np.exp(0.1 * g.standard_normal(n)).astype(np.float32)
+    U = inputs.bits_u16(inputs.weight(n, max(r, 1), seed=seed + 1, outliers=False))[:, :r]
+    V = inputs.bits_u16(inputs.weight(k, max(r, 1), seed=seed + 2, outliers=False))[:, :r]
+    return W0, s, U, V
+
+
+def test_lowrank_matches_exact_rational_sum(oracle_mod):
+    """Brute force: s*(x . w0_hat) + sum_r U[i,r] (V[:,r] . x) in rationals."""
+    n, k, r, m = 4, 32, 3, 2
+    W0, s, U, V = lowrank_case(n, k, r, 70)
+    x = inputs.bits_u16(inputs.tokens(m, k, seed=71))
+    packed, scales, ge, gd = oracle_mod.quantize(W0)
+    y = oracle_mod.gemv_lowrank(packed, scales, gd, s, U, V, x)
+    wh = exact_w_hat(packed, scales, gd)
+    xf, uf, vf = f32_of(x), f32_of(U), f32_of(V)
+    for t in range(m):
+        X = [Fraction(float(xf[t, j])) for j in range(k)]
+        proj = [sum(Fraction(float(vf[j, q])) * X[j] for j in range(k)) for q in range(r)]
+        for i in range(n):
+            base = sum(X[j] * wh[i][j] for j in range(k))
+            ex = Fraction(float(s[i])) * base + sum(Fraction(float(uf[i, q])) * proj[q] for q in range(r))
+            scale = abs(Fraction(float(s[i]))) * sum(abs(X[j] * wh[i][j]) for j in range(k)) + \
+                sum(abs(Fraction(float(uf[i, q]))) * sum(abs(Fraction(float(vf[j, q])) * X[j])
+                                                        for j in range(k)) for q in range(r))
+            assert abs(Fraction(y[t, i]) - ex) <= scale * Fraction(1, 2 ** 48)
+
+
+def test_lowrank_without_delta_is_the_scaled_gemv(oracle_mod):
+    """r = 0: s = 1 gives the block GEMV bit for bit, s = 2^j scales it exactly."""
+    n, k = 20, 96
+    W0, s, U, V = lowrank_case(n, k, 0, 72)
+    x = inputs.bits_u16(inputs.tokens(3, k, seed=73))
+    packed, scales, ge, gd = oracle_mod.quantize(W0)
+    plain = oracle_mod.gemv(packed, scales, gd, x)
+    ones = np.ones(n, np.float32)
+    assert np.array_equal(oracle_mod.gemv_lowrank(packed, scales, gd, ones, None, None, x), plain)
+    pow2 = np.float32(2.0) ** np.arange(-3, n - 3, dtype=np.float32)
+    assert np.array_equal(oracle_mod.gemv_lowrank(packed, scales, gd, pow2, None, None, x),
+                          plain * pow2.astype(np.float64))
+
+
+def test_lowrank_with_zero_block_is_the_rank_r_product(oracle_mod):
+    """W0 = 0 quantises to all-zero nibbles: only (x V) U^T remains (checked
+    against numpy's fp64 products, an independent summation)."""
+    n, k, r = 24, 128, 4
+    _, s, U, V = lowrank_case(n, k, r, 74)
+    W0 = np.zeros((n, k), np.uint16)
+    x = inputs.bits_u16(inputs.tokens(2, k, seed=75))
+    packed, scales, ge, gd = oracle_mod.quantize(W0)
+    y = oracle_mod.gemv_lowrank(packed, scales, gd, s, U, V, x)
+    ref = (f32_of(x).astype(np.float64) @ f32_of(V).astype(np.float64)) @ f32_of(U).astype(np.float64).T
+    assert np.allclose(y, ref, rtol=1e-12, atol=1e-12)
+    # U and V swapped roles (a transposed operand) would not agree
+    assert not np.allclose(y, (f32_of(x).astype(np.float64) @ f32_of(V).astype(np.float64))
+                           @ f32_of(U).astype(np.float64)[::-1].T)
