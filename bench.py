@@ -333,6 +333,62 @@ def bf16_lm_head_leg(stream, dist, a, device):
             "kernel": "gemv_bf16_kernel<1>, 8 PDL-chained calls per CUDA graph"}
 
 
+def lowrank_leg(stream, dist, a, device):
+    """The runtime low-rank GEMV (rank 4) against the plain GEMV on the ~31B
+    fused gate+up [43008, 5376] at m = 1: graphs of 8 calls alternating two
+    weight copies (260 MB, twice L2), event-timed on the launching stream."""
+    import torch
+    from nvfp4_block_scaled_aq_gb300 import aq, inputs
+    n, k = inputs.LAYER_31B[2]
+    r = 4
+    ws_w = []
+    for c in range(2):
+        W = inputs.weight(n, k, seed=inputs.seed_of(9100 + c), device=device)
+        w = aq.Nvfp4Weight.empty(n, k, device=device)
+        aq.quantize(W, w, torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8,
+                                      device=device))
+        ws_w.append(w)
+        del W
+    g = torch.Generator(device="cpu").manual_seed(9102)
+    s = torch.exp(0.1 * torch.randn(n, generator=g)).to(torch.float32).to(device)
+    U = (0.01 * torch.randn((n, r), generator=g)).to(torch.bfloat16).to(device)
+    V = (0.01 * torch.randn((k, r), generator=g)).to(torch.bfloat16).to(device)
+    x = inputs.tokens(1, k, seed=inputs.seed_of(9103), device=device)
+    y = torch.empty((1, n), dtype=torch.bfloat16, device=device)
+    ws = torch.zeros(aq.gemv_lowrank_workspace_bytes(n, k, 1, r), dtype=torch.uint8, device=device)
+    calls = 8
+
+    def graph(fn):
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            fn(0)
+            stream.synchronize()
+            with torch.cuda.graph(gr, stream=stream):
+                for i in range(calls):
+                    fn(i & 1)
+        torch.cuda.synchronize()
+
+        def run():
+            with torch.cuda.stream(stream):
+                gr.replay()
+        reps = max(3, a.steps // 10)
+        secs = time_region(run, reps, a.warmup, stream, dist) / (reps * calls)
+        del gr
+        return secs
+
+    t_lr = graph(lambda i: aq.gemv_lowrank(ws_w[i], s, U, V, x, y, ws, flags=aq.STEP_PDL,
+                                           stream=stream))
+    t_plain = graph(lambda i: aq.decode_step(aq.StepArgs([ws_w[i]], [x], [y]), ws,
+                                             flags=aq.STEP_PDL | aq.STEP_REGDECODE,
+                                             stream=stream))
+    byts = 0.5625 * n * k + 4 + 2 * k + 2 * n + 4 * n + 2 * r * (n + k)
+    return {"shape": [n, k], "r": r, "m": 1, "us_per_call": round(t_lr * 1e6, 2),
+            "GBps": round(byts / t_lr / 1e9, 1),
+            "plain_gemv_us_per_call": round(t_plain * 1e6, 2),
+            "kernels": "vx_kernel + gemv_kernel<1> (PDL) against gemv_kernel<1> alone"}
+
+
 def kernel_sha():
     h = hashlib.sha1()
     for name in ("gemv_core.cuh", "gemv.cu"):
@@ -471,6 +527,7 @@ def run_aq(a, dist):
     del g_pdl
     if not a.no_extras and a.workload == "31b":
         extras["bf16_lm_head"] = bf16_lm_head_leg(stream, dist, a, device)
+        extras["lowrank_gate_up"] = lowrank_leg(stream, dist, a, device)
 
     st = aq.poll_device_status()
     if st != aq.OK:

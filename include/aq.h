@@ -282,6 +282,37 @@ AQ_API aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj
  * AQ_ERR_INVALID_ARG, AQ_ERR_WORKSPACE before any launch; AQ_ERR_TIMEOUT
  * through aq_poll_device_status. */
 AQ_API size_t aq_gemv_bf16_workspace_bytes(int32_t n, int32_t k, int32_t m);
+
+/* The runtime low-rank GEMV: the projection evaluated from its theta bundle
+ * without rebuilding the weight (AttnQuant docs, "Throughput", "The runtime
+ * reconstruction path does not reach dense parity", and "GPU acceleration",
+ * "How the pieces fit": one kernel fuses the shared-block dot product with
+ * the low-rank delta; landing page, "How it works": W_eff = s*W0 + U V^T),
+ * with the shared block W0 quantised to NVFP4:
+ *
+ *   y[t, i] = bf16( s[i] * (g_dec * acc[t, i]) + sum_q U[i, q] * v[t, q] ),
+ *   acc[t, i] = sum_k x[t, k] * e2m1(q0[i, k]) * sd0[i, k/16] (fp32, as in
+ *   aq_gemv_nvfp4 on the register-decode kernel), v = V^T x in fp32.
+ *
+ * w0 as for aq_gemv_nvfp4 (it may be shared by every projection of a band);
+ * s fp32 [n]; U bf16 [n, r] and V bf16 [k, r] row-major (device, NULL when
+ * r == 0), 0 <= r <= AQ_LOWRANK_MAX_R; x, y, m as for aq_gemv_nvfp4 with
+ * 1 <= m <= AQ_MAX_M.  Two launches on `stream`: v = V^T x into the
+ * workspace, then the GEMV, chained with programmatic dependent launch;
+ * flags 0 or AQ_STEP_PDL (the first launch waits for the previous work on
+ * the stream programmatically).  With s = 1 and r = 0 the result equals
+ * aq_gemv_nvfp4 with AQ_PATH_GEMV_REGDECODE bit for bit.  workspace:
+ * aq_gemv_lowrank_workspace_bytes(n, k, m, r) bytes, 256-byte aligned,
+ * zero-filled once; its first aq_gemv_workspace_bytes(n, k, m) bytes follow
+ * the GEMV workspace contract, v lives after them.  Errors as for
+ * aq_gemv_nvfp4. */
+#define AQ_LOWRANK_MAX_R 16
+AQ_API size_t aq_gemv_lowrank_workspace_bytes(int32_t n, int32_t k, int32_t m, int32_t r);
+AQ_API aq_status aq_gemv_lowrank_nvfp4(const aq_nvfp4_weight *w0, const float *s,
+                                       const uint16_t *U, const uint16_t *V, int32_t r,
+                                       const uint16_t *x, int32_t m, uint16_t *y,
+                                       uint32_t flags, void *workspace,
+                                       size_t workspace_bytes, aq_stream_t stream);
 AQ_API aq_status aq_gemv_bf16(const uint16_t *w, int32_t n, int32_t k, const uint16_t *x,
                               int32_t m, uint16_t *y, uint32_t flags, void *workspace,
                               size_t workspace_bytes, aq_stream_t stream);

@@ -88,6 +88,9 @@ def _declare(L):
         "aq_gemv_nvfp4": ([W, _p, _i32, _p, C.c_int, _p, _sz, _p], C.c_int),
         "aq_gemv_nvfp4_noalloc": ([W, _p, _i32, _p, C.c_int, _p], C.c_int),
         "aq_gemv_bf16_workspace_bytes": ([_i32, _i32, _i32], _sz),
+        "aq_gemv_lowrank_workspace_bytes": ([_i32, _i32, _i32, _i32], _sz),
+        "aq_gemv_lowrank_nvfp4": ([W, _p, _p, _p, _i32, _p, _i32, _p, C.c_uint32, _p, _sz, _p],
+                                  C.c_int),
         "aq_gemv_bf16": ([_p, _i32, _i32, _p, _i32, _p, C.c_uint32, _p, _sz, _p], C.c_int),
         "aq_quantize_act_nvfp4": ([_p, _i32, _i32, _p, _p, _p, _p], C.c_int),
         "aq_decode_step_weights": ([W, _i32, C.POINTER(_p), C.POINTER(_p), _i32,
@@ -223,6 +226,27 @@ def gemv_bf16(W, x, y, workspace, flags=0, stream=None):
     check(lib().aq_gemv_bf16(_ptr(W), n, k, _ptr(x), x.shape[0], _ptr(y), flags,
                              _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream)))
+
+
+LOWRANK_MAX_R = 16  # AQ_LOWRANK_MAX_R
+
+
+def gemv_lowrank_workspace_bytes(n, k, m=1, r=0):
+    b = int(lib().aq_gemv_lowrank_workspace_bytes(n, k, m, r))
+    if b == 0:
+        raise AqError(ERR_SHAPE, last_error() or "bad low-rank GEMV shape")
+    return b
+
+
+def gemv_lowrank(w0: "Nvfp4Weight", s, U, V, x, y, workspace, flags=0, stream=None):
+    """y = s * (W0_hat x) + U (V^T x) (aq_gemv_lowrank_nvfp4); U [n, r] and
+    V [k, r] bf16, or None when r = 0."""
+    r = 0 if U is None else U.shape[1]
+    wc = w0.c()
+    check(lib().aq_gemv_lowrank_nvfp4(C.byref(wc), _ptr(s), _ptr(U), _ptr(V), r, _ptr(x),
+                                      x.shape[0], _ptr(y), flags, _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(),
+                                      _stream(stream)))
 
 
 def quantize_act(x, packed, scales, g_dec, stream=None):

@@ -333,6 +333,39 @@ aq_status aq_gemv_bf16(const uint16_t *w, int32_t n, int32_t k, const uint16_t *
                   what);
 }
 
+size_t aq_gemv_lowrank_workspace_bytes(int32_t n, int32_t k, int32_t m, int32_t r) {
+  if (check_nk(n, k) != AQ_OK || m < 1 || m > AQ_MAX_M || r < 0 || r > AQ_LOWRANK_MAX_R) return 0;
+  const DeviceInfo *dev = device_info();
+  if (!dev) return 0;
+  return gemv_lowrank_workspace_bytes(n, k, m, r, *dev);
+}
+
+aq_status aq_gemv_lowrank_nvfp4(const aq_nvfp4_weight *w0, const float *s, const uint16_t *U,
+                                const uint16_t *V, int32_t r, const uint16_t *x, int32_t m,
+                                uint16_t *y, uint32_t flags, void *workspace,
+                                size_t workspace_bytes, aq_stream_t stream) {
+  const char *what = "aq_gemv_lowrank_nvfp4";
+  aq_status st = gemv_args(w0, x, m, y, AQ_PATH_GEMV_REGDECODE, what);
+  if (st != AQ_OK) return st;
+  if (r < 0 || r > AQ_LOWRANK_MAX_R)
+    return set_error(AQ_ERR_SHAPE, "%s: r = %d outside [0, %d]", what, r, AQ_LOWRANK_MAX_R);
+  if (flags & ~AQ_STEP_PDL) return set_error(AQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", what, flags);
+  if (!s) return set_error(AQ_ERR_INVALID_ARG, "%s: s must not be NULL", what);
+  if (r > 0 && (!U || !V))
+    return set_error(AQ_ERR_INVALID_ARG, "%s: U and V must not be NULL when r > 0", what);
+  if (!aligned(s, 4) || (r > 0 && (!aligned(U, 2) || !aligned(V, 2))))
+    return set_error(AQ_ERR_ALIGNMENT, "%s: s, U, V must be naturally aligned", what);
+  const DeviceInfo *dev = device_info();
+  if (!dev) return AQ_ERR_UNSUPPORTED;
+  if ((st = check_ws(workspace, workspace_bytes,
+                     gemv_lowrank_workspace_bytes(w0->n, w0->k, m, r, *dev), what)) != AQ_OK)
+    return st;
+  return launched(launch_gemv_lowrank(*w0, s, U, V, r, x, m, y, workspace,
+                                      (flags & AQ_STEP_PDL) != 0, *dev,
+                                      reinterpret_cast<cudaStream_t>(stream)),
+                  what);
+}
+
 aq_status aq_decode_step_weights(const aq_nvfp4_weight *w, int32_t n_proj,
                                  const uint16_t *const *x, uint16_t *const *y, int32_t m,
                                  uint32_t flags, void *workspace, size_t workspace_bytes,

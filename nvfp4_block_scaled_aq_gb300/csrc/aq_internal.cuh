@@ -238,9 +238,23 @@ cudaError_t launch_gemv_bf16(const uint16_t *w, int n, int k, const uint16_t *x,
                              uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
                              cudaStream_t st);
 // Register-decode kernel only (gemv.cu).
+// The runtime low-rank epilogue terms (see Proj in gemv_core.cuh).
+struct LowRank {
+  const float *s;
+  const uint16_t *u;
+  const float *t;
+  int r;
+};
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
-                                  cudaStream_t st, const aq_nvfp4_weight *next = nullptr);
+                                  cudaStream_t st, const aq_nvfp4_weight *next = nullptr,
+                                  const LowRank *lr = nullptr);
+// y = s * (W0_hat x) + U (V^T x) (lowrank.cu): workspace and launch.
+size_t gemv_lowrank_workspace_bytes(int n, int k, int m, int r, const DeviceInfo &dev);
+cudaError_t launch_gemv_lowrank(const aq_nvfp4_weight &w0, const float *s, const uint16_t *U,
+                                const uint16_t *V, int r, const uint16_t *x, int m,
+                                uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
+                                cudaStream_t st);
 cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                  uint16_t *y, void *ws, const DeviceInfo &dev,
                                  cudaStream_t st);

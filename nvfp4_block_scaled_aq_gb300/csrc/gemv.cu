@@ -54,7 +54,7 @@ using namespace core;
 
 namespace {
 
-template <int NT>
+template <int NT, bool LR>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gemv_kernel(const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_s,
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   prefetch_x_l2(p, r.m);
   pdl_wait();  // x and the workspace may come from the previous kernel
-  consume<NT>(p, r, sv.base, ct, sv.xs, pos, aborted);
+  consume<NT, LR>(p, r, sv.base, ct, sv.xs, pos, aborted);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -157,14 +157,14 @@ bool cached_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows
   return true;
 }
 
-template <int NT>
+template <int NT, bool LR>
 cudaError_t set_smem_attr(int device) {
   static bool done[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBudget);
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, LR>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
   if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
   return e;
 }
@@ -268,7 +268,8 @@ cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint
 
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
-                                  cudaStream_t st, const aq_nvfp4_weight *next) {
+                                  cudaStream_t st, const aq_nvfp4_weight *next,
+                                  const LowRank *lr) {
   const GemvPlan plan = plan_gemv(w.n, w.k, dev);
   CUtensorMap tm_w, tm_s, tm_nw, tm_ns;
   if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
@@ -298,6 +299,12 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   p.grid = plan.grid;
   p.direct = direct_partials_fit(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
   p.scale_box = 1;
+  if (lr) {
+    p.lr_s = lr->s;
+    p.lr_u = lr->u;
+    p.lr_t = lr->t;
+    p.lr_r = lr->r;
+  }
   p.nx_w = p.nx_s = nullptr;
   p.nx_total = 0;
   p.nx_units = p.nx_grid = p.nx_pf = 0;
@@ -324,12 +331,18 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
-  if (m <= 8) {
-    if ((e = set_smem_attr<1>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  if (m <= 8 && !lr) {
+    if ((e = set_smem_attr<1, false>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, false>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  } else if (!lr) {
+    if ((e = set_smem_attr<2, false>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, false>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  } else if (m <= 8) {
+    if ((e = set_smem_attr<1, true>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, true>, tm_w, tm_s, tm_nw, tm_ns, p, r);
   } else {
-    if ((e = set_smem_attr<2>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+    if ((e = set_smem_attr<2, true>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, true>, tm_w, tm_s, tm_nw, tm_ns, p, r);
   }
   return e;
 }
@@ -385,11 +398,11 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   cfg.stream = st;
   cudaError_t e;
   if (m <= 8) {
-    if ((e = set_smem_attr<1>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1>, tm_w, tm_s, tm_w, tm_s, p, r);
+    if ((e = set_smem_attr<1, false>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, false>, tm_w, tm_s, tm_w, tm_s, p, r);
   } else {
-    if ((e = set_smem_attr<2>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2>, tm_w, tm_s, tm_w, tm_s, p, r);
+    if ((e = set_smem_attr<2, false>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, false>, tm_w, tm_s, tm_w, tm_s, p, r);
   }
   return e;
 }

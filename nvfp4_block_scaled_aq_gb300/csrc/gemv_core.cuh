@@ -105,6 +105,13 @@ struct Proj {
                             // direct_partials_fit()
   int scale_box;            // 1: each unit also loads its scale box (NVFP4);
                             // 0: the unit is the 16 KiB weight box only (bf16)
+  // Runtime low-rank form (lr_s != nullptr): y = s * (g_dec * acc) + U t,
+  // s fp32 [n], U bf16 [n, lr_r], t = V^T x fp32 [m, lr_r] (written by the
+  // launch before this one on the stream).
+  const float *lr_s;
+  const uint16_t *lr_u;
+  const float *lr_t;
+  int lr_r;
 };
 
 // The reducer of a split row block can poll the partials themselves when
@@ -196,6 +203,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
     if ((it & 1023u) == 1023u && *aborted) return false;
   }
   return false;
+}
+
+// Output value of one (row, token) before the bf16 rounding: g_dec * v, or
+// in the runtime low-rank form (LR) s[row] * (g_dec * v) + sum_q U[row, q]
+// * t[token, q], one fp32 multiply and then fused multiply-adds in q order.
+// Plain loads: t comes from the previous kernel on the stream.
+template <bool LR>
+__device__ __forceinline__ float out_value(const Proj &p, int64_t row, int token, float v,
+                                           float gd) {
+  float z = __fmul_rn(v, gd);
+  if (LR) {
+    z = __fmul_rn(p.lr_s[row], z);
+    for (int q = 0; q < p.lr_r; ++q)
+      z = __fmaf_rn(__uint_as_float(uint32_t(p.lr_u[row * p.lr_r + q]) << 16),
+                    p.lr_t[token * p.lr_r + q], z);
+  }
+  return z;
 }
 
 __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y,
@@ -402,7 +426,7 @@ __device__ __forceinline__ void prefetch_x_l2(const Proj &p, int m) {
 // it) reduces, keeping its own partial in registers and adding the others'
 // in contributor order; no barrier spans the warps, and no other
 // contributor waits.
-template <int NT>
+template <int NT, bool LR = false>
 __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t rb, bool complete,
                                             const float (&vown)[NT][4], float gd, int rg, int sg,
                                             int lane, volatile int *aborted) {
@@ -431,7 +455,7 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
       const float v = vown[nt][i];
       if (token >= m || row >= p.n) continue;
       if (complete) {
-        p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(v, gd));
+        p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<LR>(p, row, token, v, gd));
       } else if (!reducer) {
         if (direct)
           asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(
@@ -489,7 +513,7 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
             s = __fadd_rn(s, __uint_as_float(~w[q]));
             asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(r.zero + (at + q * qs)), "r"(0u) : "memory");
           }
-        p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(s, gd));
+        p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<LR>(p, row, token, s, gd));
       }
     if (!ok && !*aborted) {
       *aborted = 1;
@@ -539,7 +563,7 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
           } else {
             for (int q = 1; q < contrib; ++q) s = __fadd_rn(s, __ldcg(src + q * qs));
           }
-          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(__fmul_rn(s, gd));
+          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<LR>(p, row, token, s, gd));
         }
       __syncwarp();
       if (lane == 0) *flag = 0;
@@ -549,7 +573,7 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
 // Consumers: the whole of this CTA's share of projection p -- activation
 // staging, the unit loop, and the split-K epilogue.  Called by the kW
 // consumer warps only.
-template <int NT>
+template <int NT, bool LR = false>
 __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *base, Ctrl &ct,
                                         uint16_t *xs, RingPos &pos, volatile int *aborted) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -794,7 +818,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
         const int token = nt * 8 + 2 * c + (i & 1);
         v[nt][i] = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[min(token, 15)]);
       }
-    finish_rows<NT>(p, r, rb, complete, v, gd, rg, sg, lane, aborted);
+    finish_rows<NT, LR>(p, r, rb, complete, v, gd, rg, sg, lane, aborted);
     u += uk1 - uk0;
   }
 }

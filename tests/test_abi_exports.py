@@ -111,6 +111,19 @@ def test_host_validation_without_a_device(aq):
     assert L.aq_gemv_bf16(None, 16, 64, p16, 1, p16, 0, None, 0, None) == aq.ERR_INVALID_ARG
     assert L.aq_gemv_bf16(C.c_void_p(8), 16, 64, p16, 1, p16, 0, None, 0, None) == \
         aq.ERR_ALIGNMENT
+    # runtime low-rank GEMV: rank, s, U/V and flags checked on the host
+    lr = L.aq_gemv_lowrank_nvfp4
+    assert lr(C.byref(ok_w), p16, p16, p16, 17, p16, 1, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert lr(C.byref(ok_w), None, None, None, 0, p16, 1, p16, 0, None, 0, None) == \
+        aq.ERR_INVALID_ARG
+    assert lr(C.byref(ok_w), p16, None, p16, 4, p16, 1, p16, 0, None, 0, None) == \
+        aq.ERR_INVALID_ARG
+    assert lr(C.byref(ok_w), C.c_void_p(258), p16, p16, 4, p16, 1, p16, 0, None, 0, None) == \
+        aq.ERR_ALIGNMENT
+    assert lr(C.byref(ok_w), p16, p16, p16, 4, p16, 1, p16, 4, None, 0, None) == \
+        aq.ERR_INVALID_ARG
+    assert lr(C.byref(ok_w), p16, p16, p16, 4, p16, 17, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert L.aq_gemv_lowrank_workspace_bytes(16, 64, 1, 17) == 0
     assert L.aq_gemv_bf16_workspace_bytes(16, 12, 1) == 0
     assert L.aq_gemv_bf16_workspace_bytes(16, 64, 17) == 0
 
