@@ -65,6 +65,10 @@ def _declare(L):
     L.aqo_gemv_q.restype = None
     L.aqo_gemv_bf16.argtypes = [_p, _p, _i64, _i64, _i64, _p, _i64, _p]
     L.aqo_gemv_bf16.restype = None
+    L.aqo_gelu_tanh.argtypes = [C.c_double]
+    L.aqo_gelu_tanh.restype = C.c_double
+    L.aqo_gemv_glu.argtypes = [_p, _p, C.c_float, _p, _i64, _i64, _i64, _p, _i64, _p]
+    L.aqo_gemv_glu.restype = None
     L.aqo_gemv_lowrank.argtypes = [_p, _p, C.c_float, _p, _p, _p, _i64, _p, _i64, _i64, _i64,
                                    _p, _i64, _p]
     L.aqo_gemv_lowrank.restype = None
@@ -259,6 +263,41 @@ def gemv_lowrank(packed, scales, g_dec, s, U, V, x, rows=None):
     lib().aqo_gemv_lowrank(pp, ps, C.c_float(g_dec), pscale, pu if r else None,
                            pv if r else None, r, px, m, n, k, prow, nrows, y.ctypes.data)
     return y
+
+
+def gelu_tanh(z):
+    return float(lib().aqo_gelu_tanh(float(z)))
+
+
+def interleave_gate_up(W):
+    """Rows of the row-concatenated [gate; up] W [2f, k] in the 8-row
+    interleaved order of the fused-activation GEMV (an index permutation)."""
+    W = np.asarray(W)
+    f = W.shape[0] // 2
+    order = np.empty(2 * f, np.int64)
+    for r in range(2 * f):
+        g, i = divmod(r, 16)
+        order[r] = g * 8 + i if i < 8 else f + g * 8 + (i - 8)
+    return W[order]
+
+
+def gemv_glu(packed, scales, g_dec, x, cols=None):
+    """fp64 h [m, ncols] = gelu(y_gate) * y_up for an 8-row interleaved weight."""
+    packed, pp = _c(packed, np.uint8)
+    scales, ps = _c(scales, np.uint8)
+    x, px = _c(np.atleast_2d(x), np.uint16)
+    n = packed.shape[0]
+    m, k = x.shape
+    assert n % 16 == 0 and packed.shape == (n, k // 2) and scales.shape == (n, k // 16)
+    if cols is None:
+        ncols, pc = n // 2, None
+    else:
+        cols, pc = _c(cols, np.int64)
+        ncols = cols.size
+        assert cols.min(initial=0) >= 0 and cols.max(initial=0) < max(n // 2, 1)
+    h = np.empty((m, ncols), np.float64)
+    lib().aqo_gemv_glu(pp, ps, C.c_float(g_dec), px, m, n, k, pc, ncols, h.ctypes.data)
+    return h
 
 
 def quantize_act(x):

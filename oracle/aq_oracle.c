@@ -302,6 +302,29 @@ void aqo_gemv_lowrank(const uint8_t *packed, const uint8_t *scales, float g_dec,
   }
 }
 
+/* [G] */
+double aqo_gelu_tanh(double z) {
+  const double c = sqrt(2.0 / 3.14159265358979323846);
+  return 0.5 * z * (1.0 + tanh(c * (z + 0.044715 * z * z * z)));
+}
+
+/* [G]: the gate and up rows of output column j through the plain GEMV,
+ * then gelu(gate) * up, all in fp64. */
+void aqo_gemv_glu(const uint8_t *packed, const uint8_t *scales, float g_dec,
+                  const uint16_t *x, int64_t m, int64_t n, int64_t k,
+                  const int64_t *cols, int64_t ncols, double *h) {
+  if (cols == NULL) ncols = n / 2;
+  for (int64_t i = 0; i < ncols; ++i) {
+    const int64_t j = cols ? cols[i] : i;
+    const int64_t rows[2] = {(j / 8) * 16 + j % 8, (j / 8) * 16 + 8 + j % 8};
+    double y[2];
+    for (int64_t t = 0; t < m; ++t) {
+      aqo_gemv(packed, scales, g_dec, x + t * k, 1, n, k, rows, 2, y);
+      h[t * ncols + i] = aqo_gelu_tanh(y[0]) * y[1];
+    }
+  }
+}
+
 /* R9: every token row is quantised like a weight tensor of one row. */
 int aqo_quantize_act(const uint16_t *x, int64_t m, int64_t k, uint8_t *packed,
                      uint8_t *scales, float *g_dec) {

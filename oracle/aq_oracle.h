@@ -32,6 +32,10 @@
  *        fit" (the custom op that fuses the shared-block dot product and the
  *        low-rank delta): the runtime path evaluates s*(W0 x) + U (V^T x)
  *        instead of a rebuilt weight.
+ *   [G]  AttnQuant docs, "Throughput" (the step's elementwise work beside
+ *        the GEMVs) and Weightless docs, "Future work" ("Gate/up fusion"):
+ *        the gated MLP's h = act(gate) * up; act read as the tanh form of
+ *        GELU (the design notes' reading R15).
  *   [U]  AttnQuant docs, "GPU acceleration", "Where GPU time goes": the
  *        attention projections (when left unquantised) and the tied
  *        lm_head / embedding are bf16 weights streamed by plain GEMVs.
@@ -142,6 +146,19 @@ void aqo_gemv_lowrank(const uint8_t *packed, const uint8_t *scales, float g_dec,
                       const uint16_t *U, const uint16_t *V, int64_t r, const uint16_t *x,
                       int64_t m, int64_t n, int64_t k, const int64_t *rows, int64_t nrows,
                       double *y);
+
+/* [G] the tanh form of GELU in fp64:
+ * 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))). */
+double aqo_gelu_tanh(double z);
+
+/* [G] fused gate+up with the activation applied: the weight's rows
+ * interleave gate and up in groups of 8 (row 16j'+i gate, 16j'+8+i up, of
+ * output column j = 8j'+i); h[m, c] = gelu(y_gate) * y_up with y the fp64
+ * GEMV (aqo_gemv) of those two rows, for the selected output columns
+ * `cols` (ncols entries, or NULL for all n/2 in order).  h [m, ncols]. */
+void aqo_gemv_glu(const uint8_t *packed, const uint8_t *scales, float g_dec,
+                  const uint16_t *x, int64_t m, int64_t n, int64_t k,
+                  const int64_t *cols, int64_t ncols, double *h);
 
 /* Element-wise array forms of the five scalar conversions above (one call
  * per element, in order), so tests can sweep many values cheaply. */

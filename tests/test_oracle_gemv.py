@@ -231,3 +231,51 @@ def test_lowrank_with_zero_block_is_the_rank_r_product(oracle_mod):
     # U and V swapped roles (a transposed operand) would not agree
     assert not np.allclose(y, (f32_of(x).astype(np.float64) @ f32_of(V).astype(np.float64))
                            @ f32_of(U).astype(np.float64)[::-1].T)
+
+
+# ------------------------------------------------- fused gate+up activation
+
+def test_gelu_tanh_identities(oracle_mod):
+    """gelu(z) - gelu(-z) = z (the tanh form is odd around z/2); gelu(0) = 0;
+    within the tanh form's known distance (< 1e-3) of the exact z*Phi(z)."""
+    import math
+    assert oracle_mod.gelu_tanh(0.0) == 0.0
+    for z in (-6.0, -3.1, -1.0, -0.25, 0.5, 1.0, 2.2, 5.0, 9.0):
+        assert abs(oracle_mod.gelu_tanh(z) - oracle_mod.gelu_tanh(-z) - z) <= 1e-15 * max(1, abs(z))
+        exact = 0.5 * z * (1.0 + math.erf(z / math.sqrt(2.0)))
+        assert abs(oracle_mod.gelu_tanh(z) - exact) < 1e-3
+    assert abs(oracle_mod.gelu_tanh(12.0) - 12.0) < 1e-12
+
+
+def test_interleave_is_a_row_permutation(oracle_mod):
+    f, k = 24, 16
+    W = np.arange(2 * f * k, dtype=np.uint16).reshape(2 * f, k)
+    Wi = oracle_mod.interleave_gate_up(W)
+    assert sorted(Wi[:, 0].tolist()) == sorted(W[:, 0].tolist())
+    for j in range(f):
+        g, i = divmod(j, 8)
+        assert np.array_equal(Wi[16 * g + i], W[j])          # gate row j
+        assert np.array_equal(Wi[16 * g + 8 + i], W[f + j])  # up row j
+
+
+def test_glu_is_gelu_of_gate_times_up(oracle_mod):
+    """The fused form against the two plain GEMV rows of each column, with
+    the activation from the erf definition (error bound of the tanh form)."""
+    import math
+    f, k, m = 32, 96, 2
+    Wcat = inputs.bits_u16(inputs.weight(2 * f, k, seed=81))
+    Wi = oracle_mod.interleave_gate_up(Wcat)
+    x = inputs.bits_u16(inputs.tokens(m, k, seed=82))
+    packed, scales, ge, gd = oracle_mod.quantize(Wi)
+    h = oracle_mod.gemv_glu(packed, scales, gd, x)
+    # the interleaved tensor's quantised rows are the concatenated tensor's
+    pc, sc, gec, gdc = oracle_mod.quantize(Wcat)
+    assert gd == gdc and np.array_equal(oracle_mod.interleave_gate_up(pc), packed)
+    y = oracle_mod.gemv(pc, sc, gdc, x)   # [m, 2f] in concatenated order
+    for t in range(m):
+        for j in range(f):
+            g, u = y[t, j], y[t, f + j]
+            exact = 0.5 * g * (1.0 + math.erf(g / math.sqrt(2.0))) * u
+            assert abs(h[t, j] - exact) <= 1e-3 * abs(u) + 1e-15
+    cols = np.array([31, 0, 9])
+    assert np.array_equal(oracle_mod.gemv_glu(packed, scales, gd, x, cols=cols), h[:, cols])
