@@ -333,10 +333,12 @@ def bf16_lm_head_leg(stream, dist, a, device):
             "kernel": "gemv_bf16_kernel<1>, 8 PDL-chained calls per CUDA graph"}
 
 
-def lowrank_leg(stream, dist, a, device):
-    """The runtime low-rank GEMV (rank 4) against the plain GEMV on the ~31B
-    fused gate+up [43008, 5376] at m = 1: graphs of 8 calls alternating two
-    weight copies (260 MB, twice L2), event-timed on the launching stream."""
+def epilogue_leg(stream, dist, a, device):
+    """The GEMV's epilogue variants on the ~31B fused gate+up [43008, 5376]
+    at m = 1 -- plain, runtime low-rank (rank 4), fused activation h =
+    gelu(gate) * up -- each as a graph of 8 PDL-chained calls alternating
+    two weight copies (260 MB, twice L2), event-timed on the launching
+    stream."""
     import torch
     from nvfp4_block_scaled_aq_gb300 import aq, inputs
     n, k = inputs.LAYER_31B[2]
@@ -382,11 +384,15 @@ def lowrank_leg(stream, dist, a, device):
     t_plain = graph(lambda i: aq.decode_step(aq.StepArgs([ws_w[i]], [x], [y]), ws,
                                              flags=aq.STEP_PDL | aq.STEP_REGDECODE,
                                              stream=stream))
-    byts = 0.5625 * n * k + 4 + 2 * k + 2 * n + 4 * n + 2 * r * (n + k)
-    return {"shape": [n, k], "r": r, "m": 1, "us_per_call": round(t_lr * 1e6, 2),
-            "GBps": round(byts / t_lr / 1e9, 1),
-            "plain_gemv_us_per_call": round(t_plain * 1e6, 2),
-            "kernels": "vx_kernel + gemv_kernel<1> (PDL) against gemv_kernel<1> alone"}
+    h = torch.empty((1, n // 2), dtype=torch.bfloat16, device=device)
+    t_glu = graph(lambda i: aq.gemv_glu(ws_w[i], x, h, ws, flags=aq.STEP_PDL, stream=stream))
+    byts = 0.5625 * n * k + 4 + 2 * k + 2 * n
+    return {"shape": [n, k], "m": 1,
+            "plain_us_per_call": round(t_plain * 1e6, 2),
+            "plain_GBps": round(byts / t_plain / 1e9, 1),
+            "lowrank_r4_us_per_call": round(t_lr * 1e6, 2),
+            "glu_us_per_call": round(t_glu * 1e6, 2),
+            "kernels": "gemv_kernel<1, plain | low-rank (after vx_kernel) | GLU epilogue>"}
 
 
 def kernel_sha():
@@ -527,7 +533,7 @@ def run_aq(a, dist):
     del g_pdl
     if not a.no_extras and a.workload == "31b":
         extras["bf16_lm_head"] = bf16_lm_head_leg(stream, dist, a, device)
-        extras["lowrank_gate_up"] = lowrank_leg(stream, dist, a, device)
+        extras["gate_up_epilogues"] = epilogue_leg(stream, dist, a, device)
 
     st = aq.poll_device_status()
     if st != aq.OK:

@@ -307,6 +307,30 @@ AQ_API size_t aq_gemv_bf16_workspace_bytes(int32_t n, int32_t k, int32_t m);
  * the GEMV workspace contract, v lives after them.  Errors as for
  * aq_gemv_nvfp4. */
 #define AQ_LOWRANK_MAX_R 16
+
+/* Fused gate+up with its activation in the epilogue (the gated MLP's first
+ * half in one pass: the pages count 0.44 ms of elementwise work per 31B
+ * step beside the GEMVs, AttnQuant docs, "Throughput", where the step's
+ * time goes; and the gate+up fusion itself, "GPU acceleration", "Q/K/V
+ * fusion" and Weightless docs, "Future work", "Gate/up fusion").
+ *
+ *   h[t, j] = bf16( gelu(g_dec * acc[t, gate j]) * (g_dec * acc[t, up j]) ),
+ *   gelu(z) = 0.5 z (1 + tanh(sqrt(2/pi) (z + 0.044715 z^3))) in fp32,
+ *
+ * acc as in aq_gemv_nvfp4 on the register-decode kernel.  The weight's rows
+ * interleave gate and up in groups of 8 -- rows 16 j' .. 16 j'+7 are gate
+ * rows 8 j' .. 8 j'+7, rows 16 j'+8 .. 16 j'+15 the matching up rows -- so
+ * n = 2 f is a multiple of 16 and h is [m, f] bf16 (16-byte aligned).
+ * aq_interleave_gate_up produces that order from the row-concatenated
+ * [gate; up] bf16 weight before quantisation (a row permutation: the
+ * tensor's amax, so its per-tensor scale, and every row's bytes are those
+ * of the concatenated weight).  m, x, flags (0 or AQ_STEP_PDL), workspace
+ * (aq_gemv_workspace_bytes) and errors as for aq_gemv_nvfp4. */
+AQ_API aq_status aq_interleave_gate_up(const uint16_t *w, int32_t f, int32_t k, uint16_t *out,
+                                       aq_stream_t stream);
+AQ_API aq_status aq_gemv_glu_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m,
+                                   uint16_t *h, uint32_t flags, void *workspace,
+                                   size_t workspace_bytes, aq_stream_t stream);
 AQ_API size_t aq_gemv_lowrank_workspace_bytes(int32_t n, int32_t k, int32_t m, int32_t r);
 AQ_API aq_status aq_gemv_lowrank_nvfp4(const aq_nvfp4_weight *w0, const float *s,
                                        const uint16_t *U, const uint16_t *V, int32_t r,

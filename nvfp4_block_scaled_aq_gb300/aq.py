@@ -89,6 +89,8 @@ def _declare(L):
         "aq_gemv_nvfp4_noalloc": ([W, _p, _i32, _p, C.c_int, _p], C.c_int),
         "aq_gemv_bf16_workspace_bytes": ([_i32, _i32, _i32], _sz),
         "aq_gemv_lowrank_workspace_bytes": ([_i32, _i32, _i32, _i32], _sz),
+        "aq_interleave_gate_up": ([_p, _i32, _i32, _p, _p], C.c_int),
+        "aq_gemv_glu_nvfp4": ([W, _p, _i32, _p, C.c_uint32, _p, _sz, _p], C.c_int),
         "aq_gemv_lowrank_nvfp4": ([W, _p, _p, _p, _i32, _p, _i32, _p, C.c_uint32, _p, _sz, _p],
                                   C.c_int),
         "aq_gemv_bf16": ([_p, _i32, _i32, _p, _i32, _p, C.c_uint32, _p, _sz, _p], C.c_int),
@@ -226,6 +228,21 @@ def gemv_bf16(W, x, y, workspace, flags=0, stream=None):
     check(lib().aq_gemv_bf16(_ptr(W), n, k, _ptr(x), x.shape[0], _ptr(y), flags,
                              _ptr(workspace), workspace.numel() * workspace.element_size(),
                              _stream(stream)))
+
+
+def interleave_gate_up(W, out, stream=None):
+    """Row-concatenated [gate; up] bf16 W [2f, k] -> the 8-row interleaved
+    order of the fused-activation GEMV (aq_interleave_gate_up)."""
+    check(lib().aq_interleave_gate_up(_ptr(W), W.shape[0] // 2, W.shape[1], _ptr(out),
+                                      _stream(stream)))
+
+
+def gemv_glu(w: "Nvfp4Weight", x, h, workspace, flags=0, stream=None):
+    """h [m, n/2] = gelu(gate) * up of an interleaved fused weight (aq_gemv_glu_nvfp4)."""
+    wc = w.c()
+    check(lib().aq_gemv_glu_nvfp4(C.byref(wc), _ptr(x), x.shape[0], _ptr(h), flags,
+                                  _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                  _stream(stream)))
 
 
 LOWRANK_MAX_R = 16  # AQ_LOWRANK_MAX_R

@@ -333,6 +333,41 @@ aq_status aq_gemv_bf16(const uint16_t *w, int32_t n, int32_t k, const uint16_t *
                   what);
 }
 
+aq_status aq_interleave_gate_up(const uint16_t *w, int32_t f, int32_t k, uint16_t *out,
+                                aq_stream_t stream) {
+  const char *what = "aq_interleave_gate_up";
+  if (f < 8 || f % 8 != 0 || f > kMaxN / 2)
+    return set_error(AQ_ERR_SHAPE, "%s: f = %d must be a multiple of 8 in [8, %d]", what, f, kMaxN / 2);
+  if (k < 8 || k > kMaxK || k % 8 != 0)
+    return set_error(AQ_ERR_SHAPE, "%s: k = %d must be a multiple of 8 in [8, %d]", what, k, kMaxK);
+  if (!w || !out) return set_error(AQ_ERR_INVALID_ARG, "%s: w and out must not be NULL", what);
+  if (!aligned(w, 16) || !aligned(out, 16))
+    return set_error(AQ_ERR_ALIGNMENT, "%s: w and out must be 16-byte aligned", what);
+  return launched(launch_interleave_gate_up(w, f, k, out, reinterpret_cast<cudaStream_t>(stream)),
+                  what);
+}
+
+aq_status aq_gemv_glu_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m, uint16_t *h,
+                            uint32_t flags, void *workspace, size_t workspace_bytes,
+                            aq_stream_t stream) {
+  const char *what = "aq_gemv_glu_nvfp4";
+  aq_status st = gemv_args(w, x, m, h, AQ_PATH_GEMV_REGDECODE, what);
+  if (st != AQ_OK) return st;
+  if (w->n % 16 != 0)
+    return set_error(AQ_ERR_SHAPE, "%s: n = %d must be a multiple of 16 (gate/up row pairs)", what,
+                     w->n);
+  if (flags & ~AQ_STEP_PDL) return set_error(AQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", what, flags);
+  const DeviceInfo *dev = device_info();
+  if (!dev) return AQ_ERR_UNSUPPORTED;
+  if ((st = check_ws(workspace, workspace_bytes, gemv_workspace_bytes(w->n, w->k, *dev), what)) !=
+      AQ_OK)
+    return st;
+  return launched(launch_gemv_regdecode(*w, x, m, h, workspace, (flags & AQ_STEP_PDL) != 0, *dev,
+                                        reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr,
+                                        true),
+                  what);
+}
+
 size_t aq_gemv_lowrank_workspace_bytes(int32_t n, int32_t k, int32_t m, int32_t r) {
   if (check_nk(n, k) != AQ_OK || m < 1 || m > AQ_MAX_M || r < 0 || r > AQ_LOWRANK_MAX_R) return 0;
   const DeviceInfo *dev = device_info();

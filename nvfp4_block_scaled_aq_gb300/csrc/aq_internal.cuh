@@ -189,6 +189,8 @@ cudaError_t launch_act_quant(const uint16_t *x, int m, int k, uint8_t *packed, u
                              cudaStream_t st);
 cudaError_t launch_scales_to_canonical(const aq_nvfp4_weight &w, uint8_t *canon,
                                        cudaStream_t st);
+cudaError_t launch_interleave_gate_up(const uint16_t *w, int f, int k, uint16_t *out,
+                                      cudaStream_t st);
 
 struct GemvPlan {
   int64_t row_blocks;  // ceil(n / rows_per_block)
@@ -248,7 +250,7 @@ struct LowRank {
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
                                   cudaStream_t st, const aq_nvfp4_weight *next = nullptr,
-                                  const LowRank *lr = nullptr);
+                                  const LowRank *lr = nullptr, bool glu = false);
 // y = s * (W0_hat x) + U (V^T x) (lowrank.cu): workspace and launch.
 size_t gemv_lowrank_workspace_bytes(int n, int k, int m, int r, const DeviceInfo &dev);
 cudaError_t launch_gemv_lowrank(const aq_nvfp4_weight &w0, const float *s, const uint16_t *U,

@@ -54,7 +54,7 @@ using namespace core;
 
 namespace {
 
-template <int NT, bool LR>
+template <int NT, int EPI>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gemv_kernel(const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_s,
@@ -85,7 +85,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   prefetch_x_l2(p, r.m);
   pdl_wait();  // x and the workspace may come from the previous kernel
-  consume<NT, LR>(p, r, sv.base, ct, sv.xs, pos, aborted);
+  consume<NT, EPI>(p, r, sv.base, ct, sv.xs, pos, aborted);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -157,13 +157,13 @@ bool cached_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows
   return true;
 }
 
-template <int NT, bool LR>
+template <int NT, int EPI>
 cudaError_t set_smem_attr(int device) {
   static bool done[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, LR>,
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, EPI>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
   if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
   return e;
@@ -269,7 +269,7 @@ cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
                                   cudaStream_t st, const aq_nvfp4_weight *next,
-                                  const LowRank *lr) {
+                                  const LowRank *lr, bool glu) {
   const GemvPlan plan = plan_gemv(w.n, w.k, dev);
   CUtensorMap tm_w, tm_s, tm_nw, tm_ns;
   if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
@@ -331,18 +331,25 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
-  if (m <= 8 && !lr) {
-    if ((e = set_smem_attr<1, false>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, false>, tm_w, tm_s, tm_nw, tm_ns, p, r);
-  } else if (!lr) {
-    if ((e = set_smem_attr<2, false>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, false>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  const int epi = glu ? kEpiGlu : (lr ? kEpiLowRank : kEpiPlain);
+  if (m <= 8 && epi == kEpiPlain) {
+    if ((e = set_smem_attr<1, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiPlain>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  } else if (epi == kEpiPlain) {
+    if ((e = set_smem_attr<2, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiPlain>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  } else if (m <= 8 && epi == kEpiLowRank) {
+    if ((e = set_smem_attr<1, kEpiLowRank>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiLowRank>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  } else if (epi == kEpiLowRank) {
+    if ((e = set_smem_attr<2, kEpiLowRank>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiLowRank>, tm_w, tm_s, tm_nw, tm_ns, p, r);
   } else if (m <= 8) {
-    if ((e = set_smem_attr<1, true>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, true>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+    if ((e = set_smem_attr<1, kEpiGlu>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiGlu>, tm_w, tm_s, tm_nw, tm_ns, p, r);
   } else {
-    if ((e = set_smem_attr<2, true>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, true>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+    if ((e = set_smem_attr<2, kEpiGlu>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiGlu>, tm_w, tm_s, tm_nw, tm_ns, p, r);
   }
   return e;
 }
@@ -398,11 +405,11 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   cfg.stream = st;
   cudaError_t e;
   if (m <= 8) {
-    if ((e = set_smem_attr<1, false>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, false>, tm_w, tm_s, tm_w, tm_s, p, r);
+    if ((e = set_smem_attr<1, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiPlain>, tm_w, tm_s, tm_w, tm_s, p, r);
   } else {
-    if ((e = set_smem_attr<2, false>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, false>, tm_w, tm_s, tm_w, tm_s, p, r);
+    if ((e = set_smem_attr<2, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiPlain>, tm_w, tm_s, tm_w, tm_s, p, r);
   }
   return e;
 }

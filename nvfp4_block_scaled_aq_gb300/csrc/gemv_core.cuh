@@ -205,15 +205,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
   return false;
 }
 
+// Epilogue kinds of the register-decode kernel.
+constexpr int kEpiPlain = 0;    // y = bf16(g_dec * acc)
+constexpr int kEpiLowRank = 1;  // y = bf16(s * (g_dec * acc) + U t)
+constexpr int kEpiGlu = 2;      // h = bf16(gelu(gate) * up), rows paired in 8-row groups
+
+// GELU in its tanh form, fp32: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
+__device__ __forceinline__ float gelu_tanh(float x) {
+  const float u = __fmul_rn(0.7978845608028654f,
+                            __fmaf_rn(__fmul_rn(0.044715f, x), __fmul_rn(x, x), x));
+  return __fmul_rn(__fmul_rn(0.5f, x), __fadd_rn(1.0f, tanhf(u)));
+}
+
 // Output value of one (row, token) before the bf16 rounding: g_dec * v, or
-// in the runtime low-rank form (LR) s[row] * (g_dec * v) + sum_q U[row, q]
-// * t[token, q], one fp32 multiply and then fused multiply-adds in q order.
+// in the runtime low-rank form s[row] * (g_dec * v) + sum_q U[row, q] *
+// t[token, q], one fp32 multiply and then fused multiply-adds in q order.
 // Plain loads: t comes from the previous kernel on the stream.
-template <bool LR>
+template <int EPI>
 __device__ __forceinline__ float out_value(const Proj &p, int64_t row, int token, float v,
                                            float gd) {
   float z = __fmul_rn(v, gd);
-  if (LR) {
+  if (EPI == kEpiLowRank) {
     z = __fmul_rn(p.lr_s[row], z);
     for (int q = 0; q < p.lr_r; ++q)
       z = __fmaf_rn(__uint_as_float(uint32_t(p.lr_u[row * p.lr_r + q]) << 16),
@@ -426,7 +438,7 @@ __device__ __forceinline__ void prefetch_x_l2(const Proj &p, int m) {
 // it) reduces, keeping its own partial in registers and adding the others'
 // in contributor order; no barrier spans the warps, and no other
 // contributor waits.
-template <int NT, bool LR = false>
+template <int NT, int EPI = kEpiPlain>
 __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t rb, bool complete,
                                             const float (&vown)[NT][4], float gd, int rg, int sg,
                                             int lane, volatile int *aborted) {
@@ -445,6 +457,8 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
   const bool reducer = !complete && jj == 0;
   const bool direct = NT == 1 && p.direct;
   const int64_t zrow = (rb * (p.max_contrib - 1) - 1) * m;  // + (j * m + token) * kRB + row
+  float fin[NT][4];  // final values before rounding (GLU: stored in pairs at the end)
+  bool have = complete;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -455,7 +469,10 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
       const float v = vown[nt][i];
       if (token >= m || row >= p.n) continue;
       if (complete) {
-        p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<LR>(p, row, token, v, gd));
+        if (EPI == kEpiGlu)
+          fin[nt][i] = out_value<EPI>(p, row, token, v, gd);
+        else
+          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<EPI>(p, row, token, v, gd));
       } else if (!reducer) {
         if (direct)
           asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(
@@ -513,8 +530,12 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
             s = __fadd_rn(s, __uint_as_float(~w[q]));
             asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(r.zero + (at + q * qs)), "r"(0u) : "memory");
           }
-        p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<LR>(p, row, token, s, gd));
+        if (EPI == kEpiGlu)
+          fin[nt][i] = out_value<EPI>(p, row, token, s, gd);
+        else
+          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<EPI>(p, row, token, s, gd));
       }
+    have = ok;
     if (!ok && !*aborted) {
       *aborted = 1;
       raise_status(r.status, kDevTimeout);
@@ -563,17 +584,36 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
           } else {
             for (int q = 1; q < contrib; ++q) s = __fadd_rn(s, __ldcg(src + q * qs));
           }
-          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<LR>(p, row, token, s, gd));
+          if (EPI == kEpiGlu)
+            fin[nt][i] = out_value<EPI>(p, row, token, s, gd);
+          else
+            p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<EPI>(p, row, token, s, gd));
         }
       __syncwarp();
       if (lane == 0) *flag = 0;
     }
-  }}
+    have = ok;
+  }
+  if (EPI == kEpiGlu && have) {
+    // rows sg (gate) and sg + 8 (up) of the row group pair up: output column
+    // j = rb * 64 + rg * 8 + sg of h [m, n / 2]
+    const int64_t j = rb * (kRB / 2) + rg * 8 + sg;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int token = nt * 8 + 2 * c + i;
+        if (token >= m || 2 * j >= p.n) continue;
+        p.y[int64_t(token) * (p.n / 2) + j] =
+            f32_to_bf16_rn(__fmul_rn(gelu_tanh(fin[nt][i]), fin[nt][i + 2]));
+      }
+  }
+}
 
 // Consumers: the whole of this CTA's share of projection p -- activation
 // staging, the unit loop, and the split-K epilogue.  Called by the kW
 // consumer warps only.
-template <int NT, bool LR = false>
+template <int NT, int EPI = kEpiPlain>
 __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *base, Ctrl &ct,
                                         uint16_t *xs, RingPos &pos, volatile int *aborted) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -818,7 +858,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
         const int token = nt * 8 + 2 * c + (i & 1);
         v[nt][i] = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[min(token, 15)]);
       }
-    finish_rows<NT, LR>(p, r, rb, complete, v, gd, rg, sg, lane, aborted);
+    finish_rows<NT, EPI>(p, r, rb, complete, v, gd, rg, sg, lane, aborted);
     u += uk1 - uk0;
   }
 }

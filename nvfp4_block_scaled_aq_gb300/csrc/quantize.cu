@@ -391,6 +391,30 @@ cudaError_t launch_act_quant(const uint16_t *x, int m, int k, uint8_t *packed, u
   return cudaGetLastError();
 }
 
+// out row 16 j + i = gate row 8 j + i, out row 16 j + 8 + i = up row 8 j + i
+// (i < 8) of the row-concatenated [gate; up] weight w [2f, k]: one 16-byte
+// vector per thread, grid-stride.
+__global__ void interleave_gate_up_kernel(const uint4 *__restrict__ w, int f, int k,
+                                          uint4 *__restrict__ out) {
+  const int64_t vpr = k / 8;  // 16-byte vectors per row
+  const int64_t total = int64_t(2) * f * vpr;
+  for (int64_t v = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; v < total;
+       v += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t row = v / vpr, col = v - row * vpr;
+    const int64_t grp = row / 16, within = row % 16;
+    const int64_t src = within < 8 ? grp * 8 + within : f + grp * 8 + (within - 8);
+    out[v] = w[src * vpr + col];
+  }
+}
+
+cudaError_t launch_interleave_gate_up(const uint16_t *w, int f, int k, uint16_t *out,
+                                      cudaStream_t st) {
+  const int grid = grid_for(int64_t(2) * f * (k / 8), 256, 152 * 16);
+  interleave_gate_up_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<const uint4 *>(w), f, k,
+                                                  reinterpret_cast<uint4 *>(out));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_scales_to_canonical(const aq_nvfp4_weight &w, uint8_t *canon,
                                        cudaStream_t st) {
   const int grid = grid_for(int64_t(w.n) * (w.k / kBlock), 256, 152 * 8);

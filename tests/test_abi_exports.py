@@ -124,6 +124,14 @@ def test_host_validation_without_a_device(aq):
         aq.ERR_INVALID_ARG
     assert lr(C.byref(ok_w), p16, p16, p16, 4, p16, 17, p16, 0, None, 0, None) == aq.ERR_SHAPE
     assert L.aq_gemv_lowrank_workspace_bytes(16, 64, 1, 17) == 0
+    # fused gate+up activation: n a multiple of 16, interleave shape checks
+    w24 = aq.Nvfp4WeightC(24, 64, 256, 256, 256)
+    assert L.aq_gemv_glu_nvfp4(C.byref(w24), p16, 1, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert L.aq_gemv_glu_nvfp4(C.byref(ok_w), p16, 1, p16, 2, None, 0, None) == aq.ERR_INVALID_ARG
+    assert L.aq_interleave_gate_up(p16, 12, 64, p16, None) == aq.ERR_SHAPE
+    assert L.aq_interleave_gate_up(p16, 16, 60, p16, None) == aq.ERR_SHAPE
+    assert L.aq_interleave_gate_up(None, 16, 64, p16, None) == aq.ERR_INVALID_ARG
+    assert L.aq_interleave_gate_up(C.c_void_p(8), 16, 64, p16, None) == aq.ERR_ALIGNMENT
     assert L.aq_gemv_bf16_workspace_bytes(16, 12, 1) == 0
     assert L.aq_gemv_bf16_workspace_bytes(16, 64, 17) == 0
 
