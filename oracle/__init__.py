@@ -300,6 +300,30 @@ def gemv_glu(packed, scales, g_dec, x, cols=None):
     return h
 
 
+def quantize_segments(W, seg_end):
+    """Per-segment quantisation: each row segment [seg_end[s-1], seg_end[s])
+    of W bits through quantize() on its own.  Returns (packed [n,k/2],
+    canonical scales [n,k/16], g_dec per segment as float32 [nseg])."""
+    W = np.asarray(W)
+    parts, start = [], 0
+    for end in seg_end:
+        parts.append(quantize(W[start:end]))
+        start = end
+    packed = np.concatenate([p[0] for p in parts])
+    scales = np.concatenate([p[1] for p in parts])
+    gdec = np.array([p[3] for p in parts], np.float32)
+    return packed, scales, gdec
+
+
+def gemv_segments(packed, scales, gdec, seg_end, x):
+    """fp64 y [m, n]: each segment's rows through gemv() with its own g_dec."""
+    ys, start = [], 0
+    for s, end in enumerate(seg_end):
+        ys.append(gemv(packed[start:end], scales[start:end], float(gdec[s]), x))
+        start = end
+    return np.concatenate(ys, axis=1)
+
+
 def quantize_act(x):
     """Per-row activation quantisation: (packed [m,k/2], scales [m,k/16], g_dec [m])."""
     x, px = _c(np.atleast_2d(x), np.uint16)

@@ -279,3 +279,27 @@ def test_glu_is_gelu_of_gate_times_up(oracle_mod):
             assert abs(h[t, j] - exact) <= 1e-3 * abs(u) + 1e-15
     cols = np.array([31, 0, 9])
     assert np.array_equal(oracle_mod.gemv_glu(packed, scales, gd, x, cols=cols), h[:, cols])
+
+
+# ------------------------------------------------------ per-segment scales
+
+def test_segments_compose_the_single_tensor_functions(oracle_mod):
+    """One segment is the plain quantisation and GEMV; a segment that is an
+    exact power-of-two multiple of another quantises to the same bytes with
+    g_dec scaled by that power (the per-tensor scale follows its segment)."""
+    n1, k = 32, 96
+    A = inputs.bits_u16(inputs.weight(n1, k, seed=91))
+    p1, s1, ge1, gd1 = oracle_mod.quantize(A)
+    p, s, gd = oracle_mod.quantize_segments(A, [n1])
+    assert np.array_equal(p, p1) and np.array_equal(s, s1) and gd[0] == np.float32(gd1)
+    x = inputs.bits_u16(inputs.tokens(2, k, seed=92))
+    assert np.array_equal(oracle_mod.gemv_segments(p, s, gd, [n1], x),
+                          oracle_mod.gemv(p1, s1, gd1, x))
+    B = bf16_of(f32_of(A) * np.float32(1024.0))   # exact: a power of two
+    W = np.concatenate([A, B])
+    p2, s2, gd2 = oracle_mod.quantize_segments(W, [n1, 2 * n1])
+    assert np.array_equal(p2[:n1], p2[n1:]) and np.array_equal(s2[:n1], s2[n1:])
+    assert gd2[1] == gd2[0] * np.float32(1024.0)
+    # one scale for the whole tensor would have flattened the small segment
+    pw, sw, gew, gdw = oracle_mod.quantize(W)
+    assert not np.array_equal(pw[:n1], p2[:n1])
