@@ -308,6 +308,35 @@ AQ_API size_t aq_gemv_bf16_workspace_bytes(int32_t n, int32_t k, int32_t m);
  * aq_gemv_nvfp4. */
 #define AQ_LOWRANK_MAX_R 16
 
+/* Per-segment tensor scales for a fused weight (the quality-preserving
+ * form of the fusion: each sub-projection -- q, k, v or gate, up -- keeps
+ * the per-tensor scale it would have on its own; AttnQuant docs, "GPU
+ * acceleration", "NVFP4 quantization": checkpoints quantised projection by
+ * projection; "Q/K/V fusion" for the fused weight itself).
+ *
+ * Segments: 1 <= nseg <= AQ_MAX_SEGMENTS, seg_end a HOST array of strictly
+ * increasing row ends, seg_end[nseg-1] == n, every segment start a multiple
+ * of 16 (so each segment owns whole scale tiles).  Segment s is rows
+ * [seg_end[s-1], seg_end[s]) (seg_end[-1] = 0).
+ *
+ * aq_quantize_nvfp4_segments: each segment of W [n, k] quantised exactly as
+ * aq_quantize_nvfp4 would quantise it alone (its own amax, g_enc, g_dec),
+ * written at its rows of out->packed / out->scales; out->global_scale
+ * points to nseg floats, g_dec of segment s at index s.
+ * aq_gemv_nvfp4_segments: y[t, i] = bf16(g_dec[segment(i)] * acc[t, i]) on
+ * the register-decode kernel (acc as in aq_gemv_nvfp4); x, y, m (<=
+ * AQ_MAX_M), flags (0 or AQ_STEP_PDL), workspace and errors as there.  With
+ * one segment both equal their plain counterparts bit for bit. */
+#define AQ_MAX_SEGMENTS 8
+AQ_API aq_status aq_quantize_nvfp4_segments(const uint16_t *W, int32_t n, int32_t k,
+                                            int32_t nseg, const int32_t *seg_end,
+                                            const aq_nvfp4_weight *out, void *workspace,
+                                            size_t workspace_bytes, aq_stream_t stream);
+AQ_API aq_status aq_gemv_nvfp4_segments(const aq_nvfp4_weight *w, int32_t nseg,
+                                        const int32_t *seg_end, const uint16_t *x, int32_t m,
+                                        uint16_t *y, uint32_t flags, void *workspace,
+                                        size_t workspace_bytes, aq_stream_t stream);
+
 /* Fused gate+up with its activation in the epilogue (the gated MLP's first
  * half in one pass: the pages count 0.44 ms of elementwise work per 31B
  * step beside the GEMVs, AttnQuant docs, "Throughput", where the step's

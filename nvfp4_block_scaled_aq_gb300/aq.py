@@ -90,6 +90,10 @@ def _declare(L):
         "aq_gemv_bf16_workspace_bytes": ([_i32, _i32, _i32], _sz),
         "aq_gemv_lowrank_workspace_bytes": ([_i32, _i32, _i32, _i32], _sz),
         "aq_interleave_gate_up": ([_p, _i32, _i32, _p, _p], C.c_int),
+        "aq_quantize_nvfp4_segments": ([_p, _i32, _i32, _i32, C.POINTER(_i32), W, _p, _sz, _p],
+                                       C.c_int),
+        "aq_gemv_nvfp4_segments": ([W, _i32, C.POINTER(_i32), _p, _i32, _p, C.c_uint32, _p, _sz,
+                                    _p], C.c_int),
         "aq_gemv_glu_nvfp4": ([W, _p, _i32, _p, C.c_uint32, _p, _sz, _p], C.c_int),
         "aq_gemv_lowrank_nvfp4": ([W, _p, _p, _p, _i32, _p, _i32, _p, C.c_uint32, _p, _sz, _p],
                                   C.c_int),
@@ -143,7 +147,7 @@ class Nvfp4Weight:
     global_scale: "object"  # float32 [1]
 
     @classmethod
-    def empty(cls, n, k, device="cuda"):
+    def empty(cls, n, k, device="cuda", nscales=1):
         import torch
         pb = lib().aq_packed_bytes(n, k)
         sb = lib().aq_scale_bytes(n, k)
@@ -151,7 +155,7 @@ class Nvfp4Weight:
             raise AqError(ERR_SHAPE, "unsupported weight shape [%d, %d]" % (n, k))
         return cls(n, k, torch.empty(pb, dtype=torch.uint8, device=device),
                    torch.empty(sb, dtype=torch.uint8, device=device),
-                   torch.empty(1, dtype=torch.float32, device=device))
+                   torch.empty(nscales, dtype=torch.float32, device=device))
 
     def c(self):
         return Nvfp4WeightC(self.n, self.k, self.packed.data_ptr(),
@@ -243,6 +247,33 @@ def gemv_glu(w: "Nvfp4Weight", x, h, workspace, flags=0, stream=None):
     check(lib().aq_gemv_glu_nvfp4(C.byref(wc), _ptr(x), x.shape[0], _ptr(h), flags,
                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream)))
+
+
+MAX_SEGMENTS = 8  # AQ_MAX_SEGMENTS
+
+
+def _seg_array(seg_end):
+    return (_i32 * len(seg_end))(*[int(e) for e in seg_end])
+
+
+def quantize_segments(W, seg_end, out: "Nvfp4Weight", workspace, stream=None):
+    """Each row segment of W quantised on its own (aq_quantize_nvfp4_segments);
+    out.global_scale holds one g_dec per segment."""
+    n, k = W.shape
+    wc = out.c()
+    check(lib().aq_quantize_nvfp4_segments(_ptr(W), n, k, len(seg_end), _seg_array(seg_end),
+                                           C.byref(wc), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(),
+                                           _stream(stream)))
+
+
+def gemv_segments(w: "Nvfp4Weight", seg_end, x, y, workspace, flags=0, stream=None):
+    """y = bf16(g_dec[segment(row)] * acc) (aq_gemv_nvfp4_segments)."""
+    wc = w.c()
+    check(lib().aq_gemv_nvfp4_segments(C.byref(wc), len(seg_end), _seg_array(seg_end), _ptr(x),
+                                       x.shape[0], _ptr(y), flags, _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))
 
 
 LOWRANK_MAX_R = 16  # AQ_LOWRANK_MAX_R

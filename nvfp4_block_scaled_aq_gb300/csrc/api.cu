@@ -333,6 +333,72 @@ aq_status aq_gemv_bf16(const uint16_t *w, int32_t n, int32_t k, const uint16_t *
                   what);
 }
 
+static aq_status check_segments(int32_t n, int32_t nseg, const int32_t *seg_end,
+                                const char *what) {
+  if (nseg < 1 || nseg > AQ_MAX_SEGMENTS)
+    return set_error(AQ_ERR_SHAPE, "%s: nseg = %d outside [1, %d]", what, nseg, AQ_MAX_SEGMENTS);
+  if (!seg_end) return set_error(AQ_ERR_INVALID_ARG, "%s: seg_end is NULL", what);
+  int32_t prev = 0;
+  for (int32_t s = 0; s < nseg; ++s) {
+    if (seg_end[s] <= prev)
+      return set_error(AQ_ERR_SHAPE, "%s: seg_end must increase (segment %d)", what, s);
+    if (prev % 16 != 0)
+      return set_error(AQ_ERR_SHAPE, "%s: segment %d starts at row %d, not a multiple of 16", what,
+                       s, prev);
+    prev = seg_end[s];
+  }
+  if (prev != n)
+    return set_error(AQ_ERR_SHAPE, "%s: the last segment ends at %d, not n = %d", what, prev, n);
+  return AQ_OK;
+}
+
+aq_status aq_quantize_nvfp4_segments(const uint16_t *W, int32_t n, int32_t k, int32_t nseg,
+                                     const int32_t *seg_end, const aq_nvfp4_weight *out,
+                                     void *workspace, size_t workspace_bytes, aq_stream_t stream) {
+  const char *what = "aq_quantize_nvfp4_segments";
+  aq_status st = check_nk(n, k);
+  if (st != AQ_OK) return st;
+  if ((st = check_segments(n, nseg, seg_end, what)) != AQ_OK) return st;
+  if ((st = check_weight(out, what)) != AQ_OK) return st;
+  if (out->n != n || out->k != k)
+    return set_error(AQ_ERR_SHAPE, "%s: out is [%d, %d], input is [%d, %d]", what, out->n,
+                     out->k, n, k);
+  if (!W) return set_error(AQ_ERR_INVALID_ARG, "%s: W is NULL", what);
+  const int64_t tile_bytes = int64_t(ceil_div(k, kTileCols)) * 128;  // scales of 16 rows
+  int32_t start = 0;
+  for (int32_t s = 0; s < nseg; ++s) {
+    aq_nvfp4_weight sub = *out;
+    sub.n = seg_end[s] - start;
+    sub.packed = out->packed + int64_t(start) * (k / 2);
+    sub.scales = out->scales + int64_t(start / 16) * tile_bytes;
+    sub.global_scale = out->global_scale + s;
+    st = quantize_common(W + int64_t(start) * k, nullptr, nullptr, nullptr, sub.n, k, 0, false,
+                         &sub, workspace, workspace_bytes, stream);
+    if (st != AQ_OK) return st;
+    start = seg_end[s];
+  }
+  return AQ_OK;
+}
+
+aq_status aq_gemv_nvfp4_segments(const aq_nvfp4_weight *w, int32_t nseg, const int32_t *seg_end,
+                                 const uint16_t *x, int32_t m, uint16_t *y, uint32_t flags,
+                                 void *workspace, size_t workspace_bytes, aq_stream_t stream) {
+  const char *what = "aq_gemv_nvfp4_segments";
+  aq_status st = gemv_args(w, x, m, y, AQ_PATH_GEMV_REGDECODE, what);
+  if (st != AQ_OK) return st;
+  if ((st = check_segments(w->n, nseg, seg_end, what)) != AQ_OK) return st;
+  if (flags & ~AQ_STEP_PDL) return set_error(AQ_ERR_INVALID_ARG, "%s: unknown flags 0x%x", what, flags);
+  const DeviceInfo *dev = device_info();
+  if (!dev) return AQ_ERR_UNSUPPORTED;
+  if ((st = check_ws(workspace, workspace_bytes, gemv_workspace_bytes(w->n, w->k, *dev), what)) !=
+      AQ_OK)
+    return st;
+  return launched(launch_gemv_regdecode(*w, x, m, y, workspace, (flags & AQ_STEP_PDL) != 0, *dev,
+                                        reinterpret_cast<cudaStream_t>(stream), nullptr, nullptr,
+                                        false, nseg, seg_end),
+                  what);
+}
+
 aq_status aq_interleave_gate_up(const uint16_t *w, int32_t f, int32_t k, uint16_t *out,
                                 aq_stream_t stream) {
   const char *what = "aq_interleave_gate_up";

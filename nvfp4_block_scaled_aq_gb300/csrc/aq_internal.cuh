@@ -250,7 +250,8 @@ struct LowRank {
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
                                   cudaStream_t st, const aq_nvfp4_weight *next = nullptr,
-                                  const LowRank *lr = nullptr, bool glu = false);
+                                  const LowRank *lr = nullptr, bool glu = false,
+                                  int nseg = 0, const int32_t *seg_end = nullptr);
 // y = s * (W0_hat x) + U (V^T x) (lowrank.cu): workspace and launch.
 size_t gemv_lowrank_workspace_bytes(int n, int k, int m, int r, const DeviceInfo &dev);
 cudaError_t launch_gemv_lowrank(const aq_nvfp4_weight &w0, const float *s, const uint16_t *U,

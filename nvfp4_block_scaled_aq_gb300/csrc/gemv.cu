@@ -269,7 +269,8 @@ cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint
 cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                   uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
                                   cudaStream_t st, const aq_nvfp4_weight *next,
-                                  const LowRank *lr, bool glu) {
+                                  const LowRank *lr, bool glu, int nseg,
+                                  const int32_t *seg_end) {
   const GemvPlan plan = plan_gemv(w.n, w.k, dev);
   CUtensorMap tm_w, tm_s, tm_nw, tm_ns;
   if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
@@ -299,6 +300,10 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   p.grid = plan.grid;
   p.direct = direct_partials_fit(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
   p.scale_box = 1;
+  if (nseg > 0) {
+    p.nseg = nseg;
+    for (int i = 0; i < nseg; ++i) p.seg_end[i] = seg_end[i];
+  }
   if (lr) {
     p.lr_s = lr->s;
     p.lr_u = lr->u;
@@ -331,7 +336,7 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
-  const int epi = glu ? kEpiGlu : (lr ? kEpiLowRank : kEpiPlain);
+  const int epi = glu ? kEpiGlu : lr ? kEpiLowRank : nseg > 0 ? kEpiSegments : kEpiPlain;
   if (m <= 8 && epi == kEpiPlain) {
     if ((e = set_smem_attr<1, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiPlain>, tm_w, tm_s, tm_nw, tm_ns, p, r);
@@ -344,6 +349,12 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   } else if (epi == kEpiLowRank) {
     if ((e = set_smem_attr<2, kEpiLowRank>(dev.ordinal)) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiLowRank>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  } else if (m <= 8 && epi == kEpiSegments) {
+    if ((e = set_smem_attr<1, kEpiSegments>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiSegments>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  } else if (epi == kEpiSegments) {
+    if ((e = set_smem_attr<2, kEpiSegments>(dev.ordinal)) != cudaSuccess) return e;
+    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiSegments>, tm_w, tm_s, tm_nw, tm_ns, p, r);
   } else if (m <= 8) {
     if ((e = set_smem_attr<1, kEpiGlu>(dev.ordinal)) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiGlu>, tm_w, tm_s, tm_nw, tm_ns, p, r);

@@ -112,6 +112,10 @@ struct Proj {
   const uint16_t *lr_u;
   const float *lr_t;
   int lr_r;
+  // Per-segment tensor scales: rows [seg_end[s-1], seg_end[s]) use
+  // g_dec[s] (g_dec then points to nseg floats).
+  int nseg;
+  int seg_end[AQ_MAX_SEGMENTS];
 };
 
 // The reducer of a split row block can poll the partials themselves when
@@ -209,6 +213,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
 constexpr int kEpiPlain = 0;    // y = bf16(g_dec * acc)
 constexpr int kEpiLowRank = 1;  // y = bf16(s * (g_dec * acc) + U t)
 constexpr int kEpiGlu = 2;      // h = bf16(gelu(gate) * up), rows paired in 8-row groups
+constexpr int kEpiSegments = 3; // y = bf16(g_dec[segment(row)] * acc)
 
 // GELU in its tanh form, fp32: 0.5 x (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))).
 __device__ __forceinline__ float gelu_tanh(float x) {
@@ -224,6 +229,12 @@ __device__ __forceinline__ float gelu_tanh(float x) {
 template <int EPI>
 __device__ __forceinline__ float out_value(const Proj &p, int64_t row, int token, float v,
                                            float gd) {
+  if (EPI == kEpiSegments) {
+    int s = 0;
+#pragma unroll
+    for (int q = 0; q + 1 < AQ_MAX_SEGMENTS; ++q) s += (q + 1 < p.nseg && row >= p.seg_end[q]);
+    gd = p.g_dec[s];
+  }
   float z = __fmul_rn(v, gd);
   if (EPI == kEpiLowRank) {
     z = __fmul_rn(p.lr_s[row], z);

@@ -132,6 +132,19 @@ def test_host_validation_without_a_device(aq):
     assert L.aq_interleave_gate_up(p16, 16, 60, p16, None) == aq.ERR_SHAPE
     assert L.aq_interleave_gate_up(None, 16, 64, p16, None) == aq.ERR_INVALID_ARG
     assert L.aq_interleave_gate_up(C.c_void_p(8), 16, 64, p16, None) == aq.ERR_ALIGNMENT
+    # per-segment scales: the segment table is checked on the host
+    def segs(*e):
+        return (C.c_int32 * len(e))(*e)
+    w64 = aq.Nvfp4WeightC(64, 64, 256, 256, 256)
+    gs = L.aq_gemv_nvfp4_segments
+    assert gs(C.byref(w64), 0, segs(64), p16, 1, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert gs(C.byref(w64), 9, segs(*range(8, 72, 8)), p16, 1, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert gs(C.byref(w64), 2, segs(40, 30), p16, 1, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert gs(C.byref(w64), 2, segs(40, 64), p16, 1, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert gs(C.byref(w64), 2, segs(32, 60), p16, 1, p16, 0, None, 0, None) == aq.ERR_SHAPE
+    assert gs(C.byref(w64), 1, None, p16, 1, p16, 0, None, 0, None) == aq.ERR_INVALID_ARG
+    assert L.aq_quantize_nvfp4_segments(p16, 64, 64, 2, segs(40, 64), C.byref(w64), None, 0,
+                                        None) == aq.ERR_SHAPE
     assert L.aq_gemv_bf16_workspace_bytes(16, 12, 1) == 0
     assert L.aq_gemv_bf16_workspace_bytes(16, 64, 17) == 0
 
