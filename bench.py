@@ -42,9 +42,9 @@ NOMINAL_HBM_GBS = 8000.0  # the 8 TB/s denominator the metric names
 NCU_TRAFFIC = {
     # four launches of layer 0, m = 1, captured without cache flushing so the
     # L2 prefetch of the next projection counts where it is issued: reads
-    # 33,598,976 + 17,451,776 + 138,394,112 + 45,573,888, writes 21,870,080
+    # 33,412,352 + 16,777,216 + 141,315,072 + 43,543,296, writes 21,913,344
     # (profiles/gemv_kernel_31b_layer_dram_traffic.md)
-    ("gemma4-31b-shaped decode-step weight stream", 1, "2b9a53b5d6761bf7c8e1b5b51be7ff629fdccbe8"): 256888832,
+    ("gemma4-31b-shaped decode-step weight stream", 1, "6c2b401925a50f37aad5820b1ced175e2f7055c7"): 256961280,
 }
 
 
