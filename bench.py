@@ -43,8 +43,10 @@ NCU_TRAFFIC = {
     # four launches of layer 0, m = 1, captured without cache flushing so the
     # L2 prefetch of the next projection counts where it is issued: reads
     # 33,412,352 + 16,777,216 + 141,315,072 + 43,543,296, writes 21,913,344
-    # (profiles/gemv_kernel_31b_layer_dram_traffic.md)
-    ("gemma4-31b-shaped decode-step weight stream", 1, "6c2b401925a50f37aad5820b1ced175e2f7055c7"): 256961280,
+    # (profiles/gemv_kernel_31b_layer_dram_traffic.md); the key is of the
+    # sources after the ring wait took its poll limit as a parameter and a
+    # self-test kernel was added beside it, gemv_kernel's device code unchanged
+    ("gemma4-31b-shaped decode-step weight stream", 1, "eda968a9b0a45088039d113c78b7f735aa2cc0cd"): 256961280,
 }
 
 

@@ -405,6 +405,15 @@ AQ_API aq_status aq_step_run(const void *plan, int32_t m, void *workspace,
 AQ_API aq_status aq_scales_to_canonical(const aq_nvfp4_weight *w, uint8_t *canon,
                                  aq_stream_t stream);
 
+/* Test hook of the failure path: one kernel runs the GEMV kernels' bounded
+ * ring wait (the same device function) against a barrier that nothing
+ * completes, with at most `polls` polls (1 <= polls <= 2^20).  It gives up,
+ * records AQ_ERR_TIMEOUT in the device status word and returns; the next
+ * aq_poll_device_status reports AQ_ERR_TIMEOUT and the context stays
+ * usable.  No memory is touched.  The pages have no counterpart; it exists
+ * so the timeout path can be exercised without a fault. */
+AQ_API aq_status aq_selftest_timeout(uint32_t polls, aq_stream_t stream);
+
 /* Synchronise `stream`, read the device status word of the current device
  * and clear it.  Returns AQ_OK, AQ_ERR_RANGE or AQ_ERR_TIMEOUT (the first
  * condition recorded since the last poll), or AQ_ERR_CUDA. */

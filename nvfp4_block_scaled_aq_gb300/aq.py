@@ -90,6 +90,7 @@ def _declare(L):
         "aq_gemv_bf16_workspace_bytes": ([_i32, _i32, _i32], _sz),
         "aq_gemv_lowrank_workspace_bytes": ([_i32, _i32, _i32, _i32], _sz),
         "aq_interleave_gate_up": ([_p, _i32, _i32, _p, _p], C.c_int),
+        "aq_selftest_timeout": ([C.c_uint32, _p], C.c_int),
         "aq_quantize_nvfp4_segments": ([_p, _i32, _i32, _i32, C.POINTER(_i32), W, _p, _sz, _p],
                                        C.c_int),
         "aq_gemv_nvfp4_segments": ([W, _i32, C.POINTER(_i32), _p, _i32, _p, C.c_uint32, _p, _sz,
@@ -247,6 +248,11 @@ def gemv_glu(w: "Nvfp4Weight", x, h, workspace, flags=0, stream=None):
     check(lib().aq_gemv_glu_nvfp4(C.byref(wc), _ptr(x), x.shape[0], _ptr(h), flags,
                                   _ptr(workspace), workspace.numel() * workspace.element_size(),
                                   _stream(stream)))
+
+
+def selftest_timeout(polls=4096, stream=None):
+    """Run the bounded-wait failure path once (aq_selftest_timeout)."""
+    check(lib().aq_selftest_timeout(polls, _stream(stream)))
 
 
 MAX_SEGMENTS = 8  # AQ_MAX_SEGMENTS

@@ -399,6 +399,15 @@ aq_status aq_gemv_nvfp4_segments(const aq_nvfp4_weight *w, int32_t nseg, const i
                   what);
 }
 
+aq_status aq_selftest_timeout(uint32_t polls, aq_stream_t stream) {
+  const char *what = "aq_selftest_timeout";
+  if (polls < 1 || polls > (1u << 20))
+    return set_error(AQ_ERR_INVALID_ARG, "%s: polls = %u outside [1, 2^20]", what, polls);
+  const DeviceInfo *dev = device_info();
+  if (!dev) return AQ_ERR_UNSUPPORTED;
+  return launched(launch_selftest_wait(polls, *dev, reinterpret_cast<cudaStream_t>(stream)), what);
+}
+
 aq_status aq_interleave_gate_up(const uint16_t *w, int32_t f, int32_t k, uint16_t *out,
                                 aq_stream_t stream) {
   const char *what = "aq_interleave_gate_up";

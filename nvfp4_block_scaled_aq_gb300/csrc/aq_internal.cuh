@@ -239,6 +239,8 @@ size_t gemv_bf16_workspace_bytes(int n, int k, const DeviceInfo &dev);
 cudaError_t launch_gemv_bf16(const uint16_t *w, int n, int k, const uint16_t *x, int m,
                              uint16_t *y, void *ws, bool pdl, const DeviceInfo &dev,
                              cudaStream_t st);
+// Self-test of the bounded-wait error path (gemv.cu).
+cudaError_t launch_selftest_wait(unsigned polls, const DeviceInfo &dev, cudaStream_t st);
 // Register-decode kernel only (gemv.cu).
 // The runtime low-rank epilogue terms (see Proj in gemv_core.cuh).
 struct LowRank {

@@ -88,6 +88,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   consume<NT, EPI>(p, r, sv.base, ct, sv.xs, pos, aborted);
 }
 
+// The kernels' bounded ring wait run against an mbarrier that nothing
+// completes, with a short poll limit: it gives up, records AQ_ERR_TIMEOUT
+// in the status word and returns, exactly as a CTA whose copies never
+// arrive would.
+__global__ void selftest_wait_kernel(unsigned polls, unsigned *status) {
+  __shared__ uint64_t bar;
+  __shared__ int aborted;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    aborted = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait_n(&bar, 0, &aborted, polls)) raise_status(status, kDevTimeout);
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
 
@@ -363,6 +379,11 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
     e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiGlu>, tm_w, tm_s, tm_nw, tm_ns, p, r);
   }
   return e;
+}
+
+cudaError_t launch_selftest_wait(unsigned polls, const DeviceInfo &dev, cudaStream_t st) {
+  selftest_wait_kernel<<<1, 32, 0, st>>>(polls, dev.status);
+  return cudaGetLastError();
 }
 
 // The same launch with both tensor maps encoded on the stack for this call

@@ -190,11 +190,12 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Bounded wait for the phase with the given parity; false on give-up.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
-                                          volatile int *aborted) {
+// Bounded wait for the phase with the given parity (at most `limit` polls);
+// false on give-up.
+__device__ __forceinline__ bool mbar_wait_n(uint64_t *bar, unsigned parity,
+                                            volatile int *aborted, unsigned limit) {
   const uint32_t addr = smem_u32(bar);
-  for (unsigned it = 0; it < kSpinLimit; ++it) {
+  for (unsigned it = 0; it < limit; ++it) {
     uint32_t done;
     asm volatile(
         "{ .reg .pred p;\n"
@@ -207,6 +208,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
     if ((it & 1023u) == 1023u && *aborted) return false;
   }
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, unsigned parity,
+                                          volatile int *aborted) {
+  return mbar_wait_n(bar, parity, aborted, kSpinLimit);
 }
 
 // Epilogue kinds of the register-decode kernel.
