@@ -13,8 +13,9 @@
 // lane of the MMA warp copies them into tensor memory and issues the four
 // kind::mxf4nvf4 MMAs (M = 128, K = 64) of the unit into an fp32
 // accumulator; four epilogue warps scale by g_dec_w * g_dec_x[t], round to
-// bf16, and combine split-K partials deterministically (ticket per row
-// quarter, partials added in contributor order).  Two persistent CTAs per
+// bf16, and combine split-K partials deterministically (contributor 0
+// reduces each row quarter once the others have published; partials added
+// in contributor order).  Two persistent CTAs per
 // SM, stream-K ranges of units exactly as the register-decode GEMV.  Every wait is
 // bounded.
 #include <cudaTypedefs.h>
@@ -299,39 +300,63 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
       buf ^= 1;
       if (!ok) break;
       if (!complete) {
-        __syncwarp();
-        unsigned last = 0;
-        if (lane == 0) {
-          __threadfence();
-          last = atomicAdd(&r.tickets[rb * 4 + q], 1u) == unsigned(contrib - 1);
-          __threadfence();
-        }
-        last = __shfl_sync(0xFFFFFFFFu, last, 0);
-        if (last && row < p.n) {
-          // contributor by contributor, all tokens' loads in flight at once
-          const float *base = r.partial + rb * p.max_contrib * int64_t(a.slots) * kRB + row_local;
-          const int64_t cstride = int64_t(a.slots) * kRB;
-          for (int t0 = 0; t0 < m; t0 += 16) {
-            float acc[16];
+        // Contributor 0 (whose range ends in this row block, so usually the
+        // last to finish it) reduces each 32-row quarter once the others
+        // have published their partials with a release-add that nobody
+        // waits on; it adds every contributor's partials (its own
+        // included) in contributor order.
+        __syncwarp();  // the warp's partial stores precede lane 0's release
+        uint32_t *flag = r.tickets + rb * 4 + q;
+        if (jj != 0) {
+          if (lane == 0)
+            asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(flag) : "memory");
+        } else {
+          bool ready = true;
+          if (lane == 0) {
+            const unsigned want = unsigned(contrib - 1);
+            for (unsigned it = 0;; ++it) {
+              unsigned seen;
+              asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(flag) : "memory");
+              if (seen >= want) break;
+              if (it >= kSpinLimit || *aborted) {
+                ready = false;
+                break;
+              }
+              __nanosleep(32);
+            }
+            if (!ready && !*aborted) {
+              *aborted = 1;
+              raise_status(r.status, kDevTimeout);
+            }
+          }
+          ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+          __syncwarp();  // every lane's loads below follow lane 0's acquire
+          if (ready && row < p.n) {
+            // contributor by contributor, all tokens' loads in flight at once
+            const float *base = r.partial + rb * p.max_contrib * int64_t(a.slots) * kRB + row_local;
+            const int64_t cstride = int64_t(a.slots) * kRB;
+            for (int t0 = 0; t0 < m; t0 += 16) {
+              float acc[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-            for (int c = 0; c < contrib; ++c) {
-              float v[16];
+              for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+              for (int c = 0; c < contrib; ++c) {
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                  v[i] = t0 + i < m ? __ldcg(base + c * cstride + (t0 + i) * kRB) : 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], v[i]);
+              }
 #pragma unroll
               for (int i = 0; i < 16; ++i)
-                v[i] = t0 + i < m ? __ldcg(base + c * cstride + (t0 + i) * kRB) : 0.0f;
-#pragma unroll
-              for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], v[i]);
+                if (t0 + i < m)
+                  p.y[int64_t(t0 + i) * p.n + row] =
+                      f32_to_bf16_rn(__fmul_rn(__fmul_rn(acc[i], __ldg(a.g_dec + t0 + i)), gdw));
             }
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (t0 + i < m)
-                p.y[int64_t(t0 + i) * p.n + row] =
-                    f32_to_bf16_rn(__fmul_rn(__fmul_rn(acc[i], __ldg(a.g_dec + t0 + i)), gdw));
           }
+          __syncwarp();
+          if (ready && lane == 0) *flag = 0;
         }
-        __syncwarp();
-        if (last && lane == 0) r.tickets[rb * 4 + q] = 0;
       }
       u += uk1 - uk0;
     }
