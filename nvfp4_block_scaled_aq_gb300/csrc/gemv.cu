@@ -84,8 +84,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     return;
   }
   prefetch_x_l2(p, r.m);
-  pdl_wait();  // x and the workspace may come from the previous kernel
-  consume<NT, EPI>(p, r, sv.base, ct, sv.xs, pos, aborted);
+  // x and the workspace may come from the previous kernel: consume() waits
+  // for it once its own index work is done
+  consume<NT, EPI>(p, r, sv.base, ct, sv.xs, pos, aborted, true);
 }
 
 // The kernels' bounded ring wait run against an mbarrier that nothing

@@ -154,6 +154,15 @@ __host__ __device__ __forceinline__ int64_t owner_of(int64_t u, int64_t total, i
   return ((u + 1) * grid - 1) / total;
 }
 
+// The CTAs whose ranges meet row block rb (contrib of them) and the index
+// jj of this CTA among them (0: the one whose range ends in rb).
+__device__ __forceinline__ void row_block_share(const Proj &p, int64_t rb, int &contrib, int &jj) {
+  const int64_t unit0 = rb * p.units;
+  const int64_t own_lo = owner_of(unit0, p.total, p.grid);
+  contrib = int(owner_of(unit0 + p.units - 1, p.total, p.grid) - own_lo + 1);
+  jj = int(blockIdx.x - own_lo);
+}
+
 // Activations a CTA stages for its unit range [u_begin, u_end): the
 // `slots` distinct units of k it touches (all units if the range is at
 // least a row block long), each 256 columns, per token.
@@ -366,6 +375,8 @@ __device__ __forceinline__ bool produce(const Proj &p, uint8_t *base, Ctrl &ct, 
   if (int64_t(blockIdx.x) >= grid) return true;
   const int64_t u_begin = range_begin(blockIdx.x, p.total, grid);
   const int64_t u_end = range_begin(blockIdx.x + 1, p.total, grid);
+  int64_t rb = u_begin / p.units;  // row block and k-unit of u, advanced
+  int uk = int(u_begin - rb * p.units);  // without a division per unit
   for (int64_t u = u_begin; u < u_end; ++u, pos.advance(S)) {
     const int st = pos.st;
     // the stage was last filled one pass ago: wait for its release
@@ -377,13 +388,15 @@ __device__ __forceinline__ bool produce(const Proj &p, uint8_t *base, Ctrl &ct, 
       return false;
     }
     if (*aborted) return false;
-    const int64_t rb = u / p.units;
-    const int uk = int(u - rb * p.units);
     uint8_t *stage = base + st * kStageBytes;
     mbar_expect_tx(&ct.full[st], p.scale_box ? kStageBytes : kPackedStage);
     tma_load_2d(stage, p.tm_w, uk * kUnitCols, int(rb * kRB), &ct.full[st]);
     if (p.scale_box)
       tma_load_2d(stage + kPackedStage, p.tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[st]);
+    if (++uk == p.units) {
+      uk = 0;
+      ++rb;
+    }
   }
   return true;
 }
@@ -454,16 +467,15 @@ __device__ __forceinline__ void prefetch_x_l2(const Proj &p, int m) {
 // it) reduces, keeping its own partial in registers and adding the others'
 // in contributor order; no barrier spans the warps, and no other
 // contributor waits.
+// contrib / jj: the CTAs sharing the row block and this CTA's index among
+// them, when the caller has them already (contrib == 0: work them out).
 template <int NT, int EPI = kEpiPlain>
 __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t rb, bool complete,
                                             const float (&vown)[NT][4], float gd, int rg, int sg,
-                                            int lane, volatile int *aborted) {
+                                            int lane, volatile int *aborted, int contrib = 0,
+                                            int jj = 0) {
   const int units = p.units, m = r.m, c = lane & 3;
-  const int64_t grid = p.grid;
-  const int64_t unit0 = rb * units;
-  const int64_t own_lo = owner_of(unit0, p.total, grid);
-  const int contrib = int(owner_of(unit0 + units - 1, p.total, grid) - own_lo + 1);
-  const int jj = int(blockIdx.x - own_lo);
+  if (contrib == 0) row_block_share(p, rb, contrib, jj);
   //  * direct: the others store ~bits(partial) to the zero region and
   //    leave; the reducer polls those words (bounded) until none is zero,
   //    then puts the zeros back.
@@ -629,9 +641,12 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
 // Consumers: the whole of this CTA's share of projection p -- activation
 // staging, the unit loop, and the split-K epilogue.  Called by the kW
 // consumer warps only.
+// pdl: wait for the previous kernel on the stream (programmatic dependent
+// launch) once everything that does not read its results is worked out.
 template <int NT, int EPI = kEpiPlain>
 __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *base, Ctrl &ct,
-                                        uint16_t *xs, RingPos &pos, volatile int *aborted) {
+                                        uint16_t *xs, RingPos &pos, volatile int *aborted,
+                                        bool pdl = false) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int rg = warp;
@@ -660,33 +675,49 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
   //    row block, else the L consecutive units (mod units) from uk_begin
   const int64_t L = u_end - u_begin;
   const bool all_units = L >= units;
-  const int uk_begin = int(u_begin % units);
+  const int64_t rb0 = u_begin / units;
+  const int uk_begin = int(u_begin - rb0 * units);
   const int slots = x_slots(L, units);
   const bool full = int64_t(m) * x_stride_full(slots) <= r.x_cap;
   const int stride = full ? x_stride_full(slots) : x_stride_chunk(m);
+  // Only the first and the last row block of the range can be shared with
+  // other CTAs: their contributor counts and this CTA's index among them.
+  int contrib0, jj0, contrib1, jj1;
+  row_block_share(p, rb0, contrib0, jj0);
+  row_block_share(p, (u_end - 1) / units, contrib1, jj1);
 
   // -- per-token power-of-two shift from the largest |x| over the staged
   //    columns (a function of the token's own data and the partition only,
   //    never of m).
   const int nv_all = slots * (kUnitK / 8);  // 16-byte vectors per token
   const int per = (nv_all + kW * 32 - 1) / (kW * 32);
-  if (NT == 1 && full && m <= 2 && m * per <= 4) {
+  constexpr int kV = 4;
+  const bool in_regs = NT == 1 && full && m <= 2 && m * per <= 4;
+  int kk_of[kV];  // column of each register-staged vector (-1: none)
+#pragma unroll
+  for (int j = 0; j < kV; ++j) {
+    const int tok = j / per, v = threadIdx.x + (j - tok * per) * kW * 32;
+    kk_of[j] = -1;
+    if (in_regs && tok < m && v < nv_all) {
+      const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
+      const int uk = all_units ? s : (uk_begin + s) % units;
+      const int kk = uk * kUnitK + within;
+      if (kk < p.k) kk_of[j] = kk;
+    }
+  }
+  if (pdl) pdl_wait();
+  if (in_regs) {
     // Few vectors per thread: they stay in registers from the load to the
     // f16 store.  Each warp leaves its maximum per token in xmax[tok * kW +
     // warp]; after one barrier every thread derives the shift itself.
-    constexpr int kV = 4;
     uint4 q[kV];
     uint32_t mx0 = 0, mx1 = 0;
 #pragma unroll
     for (int j = 0; j < kV; ++j) {
-      const int tok = j / per, v = threadIdx.x + (j - tok * per) * kW * 32;
+      const int tok = j / per;
       q[j] = make_uint4(0, 0, 0, 0);
-      if (tok < m && v < nv_all) {
-        const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
-        const int uk = all_units ? s : (uk_begin + s) % units;
-        const int kk = uk * kUnitK + within;
-        if (kk < p.k) q[j] = __ldg(reinterpret_cast<const uint4 *>(p.x + int64_t(tok) * p.k + kk));
-      }
+      if (kk_of[j] >= 0)
+        q[j] = __ldg(reinterpret_cast<const uint4 *>(p.x + int64_t(tok) * p.k + kk_of[j]));
     }
 #pragma unroll
     for (int j = 0; j < kV; ++j) {
@@ -784,10 +815,9 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
   }
   const float gd = __ldg(p.g_dec);
 
-  int64_t u = u_begin;
+  int64_t u = u_begin, rb = rb0;
+  int uk0 = uk_begin;
   while (u < u_end) {
-    const int64_t rb = u / units;
-    const int uk0 = int(u - rb * units);
     const int uk1 = int(uk0 + (u_end - u) < units ? uk0 + (u_end - u) : units);
 
     float acc[2][NT][4];
@@ -874,8 +904,14 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
         const int token = nt * 8 + 2 * c + (i & 1);
         v[nt][i] = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[min(token, 15)]);
       }
-    finish_rows<NT, EPI>(p, r, rb, complete, v, gd, rg, sg, lane, aborted);
+    // (two token blocks: the shares are worked out again, which keeps
+    // their registers free through the unit loop)
+    finish_rows<NT, EPI>(p, r, rb, complete, v, gd, rg, sg, lane, aborted,
+                         NT > 1 ? 0 : complete ? 1 : (rb == rb0 ? contrib0 : contrib1),
+                         complete ? 0 : (rb == rb0 ? jj0 : jj1));
     u += uk1 - uk0;
+    ++rb;
+    uk0 = 0;
   }
 }
 
