@@ -102,6 +102,17 @@ __device__ __forceinline__ float f16_lo_to_f32(uint32_t h2) {
   return f;
 }
 
+// High f16 half of a pair -> fp32 (exact).
+__device__ __forceinline__ float f16_hi_to_f32(uint32_t h2) {
+  float f;
+  asm("{ .reg .b16 l, h;\n"
+      "  mov.b32 {l, h}, %1;\n"
+      "  cvt.f32.f16 %0, h; }"
+      : "=f"(f)
+      : "r"(h2));
+  return f;
+}
+
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));

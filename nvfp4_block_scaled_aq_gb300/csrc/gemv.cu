@@ -54,7 +54,7 @@ using namespace core;
 
 namespace {
 
-template <int NT, int EPI>
+template <int NT, int EPI, bool BD = false>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     gemv_kernel(const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_s,
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   prefetch_x_l2(p, r.m);
   // x and the workspace may come from the previous kernel: consume() waits
   // for it once its own index work is done
-  consume<NT, EPI>(p, r, sv.base, ct, sv.xs, pos, aborted, true);
+  consume<NT, EPI, BD>(p, r, sv.base, ct, sv.xs, pos, aborted, true);
 }
 
 // The kernels' bounded ring wait run against an mbarrier that nothing
@@ -174,16 +174,36 @@ bool cached_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows
   return true;
 }
 
-template <int NT, int EPI>
+template <int NT, int EPI, bool BD = false>
 cudaError_t set_smem_attr(int device) {
   static bool done[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, EPI>,
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, EPI, BD>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
   if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
   return e;
+}
+
+// One token: the block-diagonal instantiation of the epilogue kind.
+template <int EPI>
+cudaError_t launch_bd(const cudaLaunchConfig_t &cfg, const CUtensorMap &tm_w,
+                      const CUtensorMap &tm_s, const CUtensorMap &tm_nw, const CUtensorMap &tm_ns,
+                      const Proj &p, const Run &r, int device) {
+  cudaError_t e = set_smem_attr<1, EPI, true>(device);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<1, EPI, true>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+}
+cudaError_t launch_one_token(const cudaLaunchConfig_t &cfg, int epi, const CUtensorMap &tm_w,
+                             const CUtensorMap &tm_s, const CUtensorMap &tm_nw,
+                             const CUtensorMap &tm_ns, const Proj &p, const Run &r, int device) {
+  switch (epi) {
+    case kEpiLowRank: return launch_bd<kEpiLowRank>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+    case kEpiGlu: return launch_bd<kEpiGlu>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+    case kEpiSegments: return launch_bd<kEpiSegments>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+    default: return launch_bd<kEpiPlain>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+  }
 }
 
 // Activation buffer (f16) of a single-projection launch: everything the
@@ -354,6 +374,7 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   cfg.numAttrs = pdl ? 1 : 0;
   cudaError_t e;
   const int epi = glu ? kEpiGlu : lr ? kEpiLowRank : nseg > 0 ? kEpiSegments : kEpiPlain;
+  if (m == 1) return launch_one_token(cfg, epi, tm_w, tm_s, tm_nw, tm_ns, p, r, dev.ordinal);
   if (m <= 8 && epi == kEpiPlain) {
     if ((e = set_smem_attr<1, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiPlain>, tm_w, tm_s, tm_nw, tm_ns, p, r);
@@ -437,6 +458,7 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   cfg.dynamicSmemBytes = smem_bytes(r.stages, r.x_cap);
   cfg.stream = st;
   cudaError_t e;
+  if (m == 1) return launch_one_token(cfg, kEpiPlain, tm_w, tm_s, tm_w, tm_s, p, r, dev.ordinal);
   if (m <= 8) {
     if ((e = set_smem_attr<1, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiPlain>, tm_w, tm_s, tm_w, tm_s, p, r);

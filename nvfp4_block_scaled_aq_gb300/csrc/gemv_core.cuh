@@ -55,6 +55,7 @@ static_assert(kUnitCols == 128, "the swizzle pattern assumes 128-byte rows");
 struct Ctrl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
+  uint4 zero;               // 16 zero bytes: B operand of the one-token form
   uint32_t xmax[16];
   int shift[16];
   int flag;
@@ -316,6 +317,84 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// D = A * B with a zero accumulator (the first MMA of a chain).
+__device__ __forceinline__ void mma_f16_first(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+      "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%10, %10, %10, %10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// 16 bytes from shared memory.  Volatile: never moved across the barriers
+// that publish the staged activations.
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
+// One unit of one warp for a single token, with the MMA's n dimension spent
+// on blocks instead of tokens.  In k-tile t, MMA i (i = 0..7) takes element
+// pair (2i, 2i+1) of each of the tile's eight 16-element blocks: MMA column
+// pair (2c, 2c+1) carries block 2c and pair (2c+8, 2c+9) block 2c+1 of the
+// lane's 32 columns, and the activation operand is block-diagonal, B[k, j] =
+// x[k] when column k lies in block j and 0 otherwise.  After the eight MMAs
+// D[row, j] is the unscaled dot product of block j, and the lane holds rows
+// sg, sg+8 x blocks 2c, 2c+1 -- exactly the four blocks of its scale word --
+// so each block scale costs one fp32 multiply-add instead of an f16
+// multiply per weight pair.
+// acc[0][0][i]: running sums over both tiles of (row sg, block 2c),
+// (sg, 2c+1), (sg+8, 2c), (sg+8, 2c+1) of each tile.  xb[b][i]: the lane's B registers for column
+// pair (2c, 2c+1) (b = 0) or (2c+8, 2c+9) (b = 1) of MMA i: block 2c + b of
+// the token when the lane's MMA column g is 2c + b, else zero.
+// The B registers of tile t are loaded from xb_addr[b][qq] + tb[t] * xb_step[b]
+// just before the tile's MMAs.
+__device__ __forceinline__ void unit_mma_bd(float (&acc)[2][1][4], const uint4 (&wlo)[2],
+                                            const uint4 (&whi)[2], const uint32_t (&sw)[2],
+                                            const uint32_t (&xb_addr)[2][2],
+                                            const uint32_t (&xb_step)[2], const uint32_t (&tb)[2]) {
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    uint32_t xb[2][8];
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {
+        const uint4 v = lds128(xb_addr[b][qq] + tb[t] * xb_step[b]);
+        xb[b][4 * qq + 0] = v.x;
+        xb[b][4 * qq + 1] = v.y;
+        xb[b][4 * qq + 2] = v.z;
+        xb[b][4 * qq + 3] = v.w;
+      }
+    float d[4];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t fl[4], fh[4], gl[4], gh[4];
+      e2m1x8_to_f16x2x4(hh ? wlo[t].y : wlo[t].x, fl);  // row sg, block 2c
+      e2m1x8_to_f16x2x4(hh ? whi[t].y : whi[t].x, fh);  // row sg+8, block 2c
+      e2m1x8_to_f16x2x4(hh ? wlo[t].w : wlo[t].z, gl);  // row sg, block 2c+1
+      e2m1x8_to_f16x2x4(hh ? whi[t].w : whi[t].z, gh);  // row sg+8, block 2c+1
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t A[4] = {fl[j], fh[j], gl[j], gh[j]};
+        if (hh == 0 && j == 0)
+          mma_f16_first(d, A, xb[0][0], xb[1][0]);
+        else
+          mma_f16(d, A, xb[0][4 * hh + j], xb[1][4 * hh + j]);
+      }
+    }
+    const uint32_t s01 = e4m3x2_to_f16x2(uint16_t(sw[t] & 0xFFFFu));
+    const uint32_t s23 = e4m3x2_to_f16x2(uint16_t(sw[t] >> 16));
+    acc[0][0][0] = __fmaf_rn(d[0], f16_lo_to_f32(s01), acc[0][0][0]);
+    acc[0][0][1] = __fmaf_rn(d[1], f16_hi_to_f32(s01), acc[0][0][1]);
+    acc[0][0][2] = __fmaf_rn(d[2], f16_lo_to_f32(s23), acc[0][0][2]);
+    acc[0][0][3] = __fmaf_rn(d[3], f16_hi_to_f32(s23), acc[0][0][3]);
+  }
 }
 
 // One unit of one warp: both k-tiles, MMAs of the two tiles interleaved.
@@ -643,10 +722,12 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
 // consumer warps only.
 // pdl: wait for the previous kernel on the stream (programmatic dependent
 // launch) once everything that does not read its results is worked out.
-template <int NT, int EPI = kEpiPlain>
+// BD: one token (NT == 1, m == 1) in the block-diagonal form of unit_mma_bd.
+template <int NT, int EPI = kEpiPlain, bool BD = false>
 __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *base, Ctrl &ct,
                                         uint16_t *xs, RingPos &pos, volatile int *aborted,
                                         bool pdl = false) {
+  static_assert(!BD || NT == 1, "the block-diagonal form serves one token");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int rg = warp;
@@ -815,6 +896,23 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
   }
   const float gd = __ldg(p.g_dec);
 
+  // block-diagonal B operand: a lane whose MMA column g is block 2c + b of
+  // its columns loads that block's two staged sub-blocks (address
+  // xb_addr[b][qq] + the tile's offset); every other load of the lane reads
+  // the 16 zero bytes of the control block (the tile offset times zero)
+  uint32_t xb_addr[2][2], xb_step[2];
+  if constexpr (BD) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const bool act = g == 2 * c + b;
+      xb_step[b] = act ? 1u : 0u;
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq)
+        xb_addr[b][qq] = act ? smem_u32(xs) + 64 * c + 16 * ((2 * b + qq) ^ (c & 2))
+                             : smem_u32(&ct.zero);
+    }
+  }
+
   int64_t u = u_begin, rb = rb0;
   int uk0 = uk_begin;
   while (u < u_end) {
@@ -869,6 +967,13 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
         __syncwarp();
         if (lane == 0) mbar_arrive(&ct.empty[st]);
 
+        if constexpr (BD) {
+          const uint32_t tb[2] = {uint32_t(slot * kKT) * (kTileHalves * 2),
+                                  uint32_t(slot * kKT + 1) * (kTileHalves * 2)};
+          unit_mma_bd(acc, wlo, whi, sw, xb_addr, xb_step, tb);
+          continue;
+        }
+
         // -- activations of the unit's two k-tiles for each n8 block of tokens
         uint32_t xr[2][NT][16];
 #pragma unroll
@@ -897,13 +1002,26 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
     //    the two k-tile accumulators are added in a fixed order
     const bool complete = (uk0 == 0 && uk1 == units);
     float v[NT][4];
+    if constexpr (BD) {
+      // rows sg and sg+8: the lane's two block columns, then the four lanes
+      // of the quad (all four end with the same sums)
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int token = nt * 8 + 2 * c + (i & 1);
-        v[nt][i] = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[min(token, 15)]);
+      for (int h = 0; h < 2; ++h) {
+        float rs = __fadd_rn(acc[0][0][2 * h], acc[0][0][2 * h + 1]);
+        rs = __fadd_rn(rs, __shfl_xor_sync(0xFFFFFFFFu, rs, 1));
+        rs = __fadd_rn(rs, __shfl_xor_sync(0xFFFFFFFFu, rs, 2));
+        v[0][2 * h] = mul_pow2(rs, -ct.shift[0]);
+        v[0][2 * h + 1] = 0.0f;  // token 1: not present
       }
+    } else {
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int token = nt * 8 + 2 * c + (i & 1);
+          v[nt][i] = mul_pow2(__fadd_rn(acc[0][nt][i], acc[1][nt][i]), -ct.shift[min(token, 15)]);
+        }
+    }
     // (two token blocks: the shares are worked out again, which keeps
     // their registers free through the unit loop)
     finish_rows<NT, EPI>(p, r, rb, complete, v, gd, rg, sg, lane, aborted,
@@ -935,6 +1053,7 @@ __device__ __forceinline__ void init_ring(Ctrl &ct, int S) {
     mbar_init(&ct.empty[s], kW);
   }
   ct.aborted = 0;
+  ct.zero = make_uint4(0, 0, 0, 0);
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 

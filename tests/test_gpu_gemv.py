@@ -65,17 +65,27 @@ def test_gemv_fused_qkv_config_exact_rounding_rate():
 @pytest.mark.parametrize("n,k", [(1152, 6912), (13824, 1152)])
 def test_gemv_is_independent_of_m(kernel, n, k):
     """On each kernel, each token's output is bit-identical whatever else
-    is in the batch."""
+    is in the batch, for batches of two or more.  A single token on the
+    register-decode kernel takes its one-token form (block sums on the MMA's
+    n dimension, a different fp32 summation order): it is held to the
+    oracle instead, like every other output."""
     path, max_m = KERNELS[kernel]
-    w = quantize_gpu(inputs.weight(n, k, seed=5, device=DEV))
+    W = inputs.weight(n, k, seed=5, device=DEV)
+    w = quantize_gpu(W)
     x = inputs.tokens(max_m, k, seed=6, device=DEV)
     y_all = gemv_gpu(w, x, path=path)
+    one_token_form = kernel == "regdecode"
     for m in sorted({1, 2, 3, 8, 9, max_m}):
-        if m <= max_m:
+        if m <= max_m and not (m == 1 and one_token_form):
             ym = gemv_gpu(w, x[:m].contiguous(), path=path)
             assert torch.equal(ym, y_all[:m]), m
-    for t in sorted({0, max_m // 2, max_m - 1}):
-        assert torch.equal(gemv_gpu(w, x[t:t + 1].contiguous(), path=path)[0], y_all[t])
+    ts = sorted({0, max_m // 2, max_m - 1})
+    singles = torch.stack([gemv_gpu(w, x[t:t + 1].contiguous(), path=path)[0] for t in ts])
+    if one_token_form:
+        assert_gemv_close(singles, oracle_y(W, x[ts]), "single tokens")
+        assert_gemv_close(y_all[ts], oracle_y(W, x[ts]), "batched")
+    else:
+        assert torch.equal(singles, y_all[ts])
 
 
 def test_gemv_is_deterministic_and_workspace_rearms():

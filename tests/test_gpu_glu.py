@@ -58,13 +58,19 @@ def test_glu_matches_oracle(f, k, m):
 
 
 def test_glu_is_independent_of_m():
+    """Bit-identical per token for batches of two or more; one token (the
+    one-token kernel form) within tolerance of the oracle."""
     f, k = 520, 4096
-    w = quantize_gpu(interleaved(inputs.weight(2 * f, k, seed=9301, device=DEV)))
+    Wi = interleaved(inputs.weight(2 * f, k, seed=9301, device=DEV))
+    w = quantize_gpu(Wi)
     x = inputs.tokens(16, k, seed=9302, device=DEV)
     h16 = glu_gpu(w, x)
     assert torch.equal(glu_gpu(w, x), h16)
-    for m in (1, 3, 9):
+    for m in (2, 3, 9):
         assert torch.equal(glu_gpu(w, x[:m].contiguous(), flags=aq.STEP_PDL), h16[:m]), m
+    packed, scales, ge, gd = oracle.quantize(bits(Wi))
+    h_ref = oracle.gemv_glu(packed, scales, gd, bits(x[:1]))
+    assert_gemv_close(glu_gpu(w, x[:1].contiguous(), flags=aq.STEP_PDL), h_ref, "one token")
 
 
 def test_glu_31b_gate_up_sampled_parity():

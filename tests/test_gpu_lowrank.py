@@ -71,8 +71,8 @@ def test_lowrank_without_delta_equals_the_gemv(m):
 
 
 def test_lowrank_band_shares_one_block_and_is_independent_of_m():
-    """Three bundles of one band share W0; each matches the oracle, and each
-    token's output equals its m = 1 call bit for bit."""
+    """Three bundles of one band share W0; each matches the oracle, and so
+    does each token's single-token call (the one-token kernel form)."""
     n, k, r = 1536, 1152, 4
     W0 = inputs.weight(n, k, seed=8401, device=DEV)
     w0 = quantize_gpu(W0)
@@ -80,7 +80,9 @@ def test_lowrank_band_shares_one_block_and_is_independent_of_m():
     for layer in range(3):
         s, U, V = bundle(n, k, r, 8410 + layer)
         y = lowrank_gpu(w0, s, U, V, x)
-        assert_gemv_close(y, oracle_lowrank(W0, s, U, V, x), "band layer %d" % layer)
+        y_ref = oracle_lowrank(W0, s, U, V, x)
+        assert_gemv_close(y, y_ref, "band layer %d" % layer)
         for t in (0, 5):
-            assert torch.equal(lowrank_gpu(w0, s, U, V, x[t:t + 1].contiguous(),
-                                           flags=aq.STEP_PDL)[0], y[t])
+            y1 = lowrank_gpu(w0, s, U, V, x[t:t + 1].contiguous(), flags=aq.STEP_PDL)
+            assert_gemv_close(y1, y_ref[t:t + 1], "band layer %d token %d" % (layer, t))
+        assert torch.equal(lowrank_gpu(w0, s, U, V, x[2:5].contiguous()), y[2:5])

@@ -88,6 +88,11 @@ def test_one_segment_is_the_plain_path_and_m_invariant():
     seg = [512, 1024, 1536]
     w3 = quantize_segments_gpu(qkv_like(seg, k, 9803), seg)
     y3 = gemv_segments_gpu(w3, seg, x)
-    for m in (1, 5):
+    for m in (2, 5):
         assert torch.equal(gemv_segments_gpu(w3, seg, x[:m].contiguous(), flags=aq.STEP_PDL),
                            y3[:m])
+    # one token: the one-token kernel form, held to the oracle
+    W3 = qkv_like(seg, k, 9803)
+    packed, scales, gdec = oracle.quantize_segments(bits(W3), seg)
+    assert_gemv_close(gemv_segments_gpu(w3, seg, x[:1].contiguous(), flags=aq.STEP_PDL),
+                      oracle.gemv_segments(packed, scales, gdec, seg, bits(x[:1])), "one token")

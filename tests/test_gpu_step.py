@@ -122,13 +122,23 @@ def test_persistent_step_repeats_bit_exact_and_is_m_invariant():
     torch.cuda.synchronize()
     for a, b in zip(ys4, first):
         assert torch.equal(a, b)
+    # two of the four tokens alone: the same bits
+    xs2 = [x[2:4].contiguous() for x in xs4]
+    ys2 = [torch.empty((2, y.shape[1]), dtype=torch.bfloat16, device=DEV) for y in ys4]
+    plan2 = aq.StepPlan(ws, xs2, ys2)
+    aq.step_run(plan2, plan2.workspace())
+    torch.cuda.synchronize()
+    for a, b in zip(ys2, first):
+        assert torch.equal(a, b[2:4])
+    # one token takes the one-token kernel form: held to the oracle
     xs1 = [x[2:3].contiguous() for x in xs4]
     ys1 = [torch.empty((1, y.shape[1]), dtype=torch.bfloat16, device=DEV) for y in ys4]
     plan1 = aq.StepPlan(ws, xs1, ys1)
     aq.step_run(plan1, plan1.workspace())
     torch.cuda.synchronize()
-    for a, b in zip(ys1, first):
-        assert torch.equal(a[0], b[2])
+    for i, (W, x, a) in enumerate(zip(Ws, xs1, ys1)):
+        packed, scales, ge, gd = oracle.quantize(bits(W))
+        assert_gemv_close(a, oracle.gemv(packed, scales, gd, bits(x)), "one token, projection %d" % i)
     assert aq.poll_device_status() == aq.OK
 
 
