@@ -40,13 +40,12 @@ NOMINAL_HBM_GBS = 8000.0  # the 8 TB/s denominator the metric names
 # capture), keyed by the workload and the sha1 of the GEMV kernel sources the
 # capture was taken on; when they change the figure no longer applies (null).
 NCU_TRAFFIC = {
-    # four launches of layer 0, m = 1, captured without cache flushing so the
-    # L2 prefetch of the next projection counts where it is issued: reads
-    # 33,412,352 + 16,777,216 + 141,315,072 + 43,543,296, writes 21,913,344
-    # (profiles/gemv_kernel_31b_layer_dram_traffic.md); the key is of the
-    # sources after the ring wait took its poll limit as a parameter and a
-    # self-test kernel was added beside it, gemv_kernel's device code unchanged
-    ("gemma4-31b-shaped decode-step weight stream", 1, "eda968a9b0a45088039d113c78b7f735aa2cc0cd"): 256961280,
+    # four launches of layer 0, m = 1 (the one-token kernel form), captured
+    # without cache flushing so the L2 prefetch of the next projection counts
+    # where it is issued: reads 33,095,168 + 17,652,736 + 136,357,888 +
+    # 47,911,936, writes 213,504 + 87,552 + 22,068,992 + 173,312
+    # (profiles/gemv_kernel_31b_layer_dram_traffic.md)
+    ("gemma4-31b-shaped decode-step weight stream", 1, "48a88e11e5d92072b77e6327d56df4395f41acc3"): 257561088,
 }
 
 

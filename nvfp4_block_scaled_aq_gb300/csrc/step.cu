@@ -120,7 +120,7 @@ __device__ __forceinline__ Proj with_next(Proj p, const StepProj &n) {
   return p;
 }
 
-template <int NT, bool BD = false>
+template <int NT>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     step_kernel(const uint8_t *__restrict__ plan, uint8_t *ws, uint64_t ws_bytes, int m,
                 unsigned *status) {
@@ -162,17 +162,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   for (int p = 0; p < h.n_proj; ++p) {
     if (p > 0) grid_barrier(bar, gridDim.x, aborted, status);
     if (*aborted) break;
-    consume<NT, kEpiPlain, BD>(to_proj(projs[p]), r, sv.base, ct, sv.xs, pos, aborted);
+    consume<NT>(to_proj(projs[p]), r, sv.base, ct, sv.xs, pos, aborted);
   }
 }
 
-template <int NT, bool BD = false>
+template <int NT>
 cudaError_t set_step_smem_attr(int device) {
   static bool done[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(step_kernel<NT, BD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(step_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBudget);
   if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
   return e;
@@ -262,10 +262,7 @@ cudaError_t launch_step(const void *plan, int m, void *ws, size_t ws_bytes, cons
   const uint8_t *pl = static_cast<const uint8_t *>(plan);
   uint8_t *w = static_cast<uint8_t *>(ws);
   cudaError_t e;
-  if (m == 1) {
-    if ((e = set_step_smem_attr<1, true>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, step_kernel<1, true>, pl, w, uint64_t(ws_bytes), m, dev.status);
-  } else if (m <= 8) {
+  if (m <= 8) {
     if ((e = set_step_smem_attr<1>(dev.ordinal)) != cudaSuccess) return e;
     e = cudaLaunchKernelEx(&cfg, step_kernel<1>, pl, w, uint64_t(ws_bytes), m, dev.status);
   } else {
