@@ -266,12 +266,18 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev) {
   p.k_tiles = ceil_div(k, kTileCols);
   p.units = ceil_div(p.k_tiles, kKT);
   p.total = p.row_blocks * p.units;
-  // Two persistent CTAs per SM (the shared-memory budget of each CTA is set
-  // so both are resident); tiny projections get one unit per CTA.  The
-  // grid depends only on (n, k) and the SM count, never on m.
+  // Up to two persistent CTAs per SM (the shared-memory budget of each CTA
+  // is set so both are resident); tiny projections get one unit per CTA.
+  // Of the grids whose longest range is as short as two CTAs per SM allow,
+  // the smallest: every range then has that length (or one unit less), so
+  // no CTA idles while others finish an extra unit, and fewer CTAs share
+  // each split row block.  The grid depends only on (n, k) and the SM
+  // count, never on m.
   int64_t g = int64_t(dev.sms) * kCtasPerSm;
   if (g > p.total) g = p.total;
   if (g < 1) g = 1;
+  const int64_t longest = (p.total + g - 1) / g;
+  g = (p.total + longest - 1) / longest;
   p.grid = int(g);
   int worst = 1;
   for (int64_t rb = 0; rb < p.row_blocks; ++rb) {
