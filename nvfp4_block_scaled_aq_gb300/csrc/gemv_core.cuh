@@ -269,6 +269,26 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// The same copy with an L2 eviction-priority hint (a policy made by
+// createpolicy): the weight stream is read once per step, so its lines go
+// in at evict_first and leave L2 to what is read again soon -- the
+// activations, the split-K partials and the next projection's prefetched
+// first units.
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map, int x, int y,
+                                                 uint64_t *bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
 // Consumer-warps-only barrier (the producer warp never joins it).
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kW * 32) : "memory");
@@ -456,6 +476,7 @@ __device__ __forceinline__ bool produce(const Proj &p, uint8_t *base, Ctrl &ct, 
   const int64_t u_end = range_begin(blockIdx.x + 1, p.total, grid);
   int64_t rb = u_begin / p.units;  // row block and k-unit of u, advanced
   int uk = int(u_begin - rb * p.units);  // without a division per unit
+  const uint64_t policy = l2_evict_first_policy();
   for (int64_t u = u_begin; u < u_end; ++u, pos.advance(S)) {
     const int st = pos.st;
     // the stage was last filled one pass ago: wait for its release
@@ -469,9 +490,10 @@ __device__ __forceinline__ bool produce(const Proj &p, uint8_t *base, Ctrl &ct, 
     if (*aborted) return false;
     uint8_t *stage = base + st * kStageBytes;
     mbar_expect_tx(&ct.full[st], p.scale_box ? kStageBytes : kPackedStage);
-    tma_load_2d(stage, p.tm_w, uk * kUnitCols, int(rb * kRB), &ct.full[st]);
+    tma_load_2d_hint(stage, p.tm_w, uk * kUnitCols, int(rb * kRB), &ct.full[st], policy);
     if (p.scale_box)
-      tma_load_2d(stage + kPackedStage, p.tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[st]);
+      tma_load_2d_hint(stage + kPackedStage, p.tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[st],
+                       policy);
     if (++uk == p.units) {
       uk = 0;
       ++rb;
