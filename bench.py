@@ -40,12 +40,13 @@ NOMINAL_HBM_GBS = 8000.0  # the 8 TB/s denominator the metric names
 # capture), keyed by the workload and the sha1 of the GEMV kernel sources the
 # capture was taken on; when they change the figure no longer applies (null).
 NCU_TRAFFIC = {
-    # four launches of layer 0, m = 1 (the one-token kernel form), captured
-    # without cache flushing so the L2 prefetch of the next projection counts
-    # where it is issued: reads 33,095,168 + 17,652,736 + 136,357,888 +
-    # 47,911,936, writes 213,504 + 87,552 + 22,068,992 + 173,312
-    # (profiles/gemv_kernel_31b_layer_dram_traffic.md)
-    ("gemma4-31b-shaped decode-step weight stream", 1, "48a88e11e5d92072b77e6327d56df4395f41acc3"): 257561088,
+    # the four launches of one layer (layer 3 of an 8-layer stream, so no
+    # weight of the layer can still sit in L2 from an earlier step), m = 1,
+    # one-token kernel form, captured without cache flushing so the L2
+    # prefetch of the next projection counts where it is issued: reads
+    # 19,086,336 + 15,315,456 + 142,870,272 + 68,184,064, writes 91,136 +
+    # 77,824 + 408,576 + 165,376 (profiles/gemv_kernel_31b_layer_dram_traffic.md)
+    ("gemma4-31b-shaped decode-step weight stream", 1, "0df16390a71c1ecacba701146e9130d0f7b99cc0"): 246199040,
 }
 
 
