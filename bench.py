@@ -45,8 +45,10 @@ NCU_TRAFFIC = {
     # one-token kernel form, captured without cache flushing so the L2
     # prefetch of the next projection counts where it is issued: reads
     # 19,086,336 + 15,315,456 + 142,870,272 + 68,184,064, writes 91,136 +
-    # 77,824 + 408,576 + 165,376 (profiles/gemv_kernel_31b_layer_dram_traffic.md)
-    ("gemma4-31b-shaped decode-step weight stream", 1, "0df16390a71c1ecacba701146e9130d0f7b99cc0"): 246199040,
+    # 77,824 + 408,576 + 165,376 (profiles/gemv_kernel_31b_layer_dram_traffic.md);
+    # the key is of the sources after comment-only edits to gemv.cu, the
+    # device code unchanged since the capture
+    ("gemma4-31b-shaped decode-step weight stream", 1, "83e96172c032b4ac9ada6f291548c27441508458"): 246199040,
 }
 
 

@@ -181,10 +181,12 @@ AQ_API size_t aq_gemv_workspace_bytes(int32_t n, int32_t k, int32_t m);
  * bf16 and y [m, n] bf16 row-major, 16-byte aligned, y not overlapping x.
  * The result does not depend on timing (the split over the K axis is fixed
  * by (n, k) and its partial sums are added in a fixed order), and, within
- * one kernel, not on m: each token's output equals its m = 1 call bit for
- * bit for every m the kernel serves (1..5 on the tcgen05 kernel, 1..16 on
- * the register-decode kernel).  Both kernels meet the same tolerance
- * against the exact product. */
+ * one kernel, not on the rest of the batch: on the tcgen05 kernel each
+ * token's output equals its m = 1 call bit for bit (m = 1..5); on the
+ * register-decode kernel it is the same bits for every m = 2..16, while a
+ * single token (m = 1) takes that kernel's one-token form, whose fp32 sums
+ * run in a different order.  Every form meets the same tolerance against
+ * the exact product. */
 AQ_API aq_status aq_gemv_nvfp4(const aq_nvfp4_weight *w, const uint16_t *x, int32_t m,
                         uint16_t *y, aq_path path, void *workspace,
                         size_t workspace_bytes, aq_stream_t stream);

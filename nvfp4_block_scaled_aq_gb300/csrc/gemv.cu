@@ -12,8 +12,11 @@
 //    of scale words.  Tall boxes keep HBM efficient even though each CTA
 //    streams its own contiguous range of units.
 //  * Units are laid out row-block-major and cut into equal contiguous
-//    ranges, one per persistent CTA (stream-K), two CTAs per SM, so every
-//    CTA streams the same number of bytes whatever the shape.
+//    ranges, one per persistent CTA (stream-K), at most two CTAs per SM, so
+//    every CTA streams the same number of bytes whatever the shape; the
+//    grid is the smallest that keeps the longest range as short as two
+//    CTAs per SM allow (plan_gemv), so the ranges are equal to within one
+//    unit and a split row block has as few contributors as possible.
 //  * One producer warp streams units into a ring of 2..6 stages (as many as
 //    the shared-memory budget allows after the activations); it runs ahead
 //    of the programmatic-dependent-launch wait, so the next projection's
@@ -29,16 +32,24 @@
 //    operand, so 1..16 tokens share every decoded weight fragment.  The
 //    column order inside an MMA k16 step is a permutation of the tile's
 //    columns applied identically to weights and activations.
+//  * One token (m = 1): the MMA's n dimension carries the tile's eight
+//    16-element blocks instead of tokens (block-diagonal activation
+//    operand), so D holds unscaled block sums and each block scale is one
+//    fp32 multiply-add on them instead of an f16 multiply per weight pair
+//    (unit_mma_bd in gemv_core.cuh).
 //  * Each CTA stages only the activation columns its units touch, as f16
 //    after an exact power-of-two rescale that puts each token's largest |x|
 //    over those columns in [2^14, 2^15); bf16 values keep all 8 significand
 //    bits in f16 there (only values 2^29 below the maximum round), and the
 //    partial sums are scaled back exactly.
-//  * Split-K across CTAs is deterministic: each contributor writes its fp32
-//    partial to the workspace, the last to arrive (atomic ticket per row
-//    block) adds the partials in contributor order and writes bf16 y, then
-//    re-arms the ticket.  The partition depends only on (n, k) and the SM
-//    count, never on m, so each token's result is independent of m.
+//  * Split-K across CTAs is deterministic: contributor 0 of a split row
+//    block (the CTA whose range ends in it) adds the others' fp32 partials
+//    in contributor order and writes bf16 y (finish_rows in gemv_core.cuh).
+//    The partition depends only on (n, k) and the SM count, never on m, so
+//    for m >= 2 each token's result is independent of the rest of the batch.
+//  * The weight copies carry an evict-first L2 policy: the stream is read
+//    once per step and leaves L2 to the activations, partials and the next
+//    projection's prefetched units.
 //  * Every mbarrier wait is bounded; a wait that gives up records
 //    AQ_ERR_TIMEOUT in the device status word and the CTA winds down.
 #include <cudaTypedefs.h>
