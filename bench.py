@@ -14,6 +14,7 @@ per-tensor scale + activations in + outputs out) and ms per step.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl aq|reference]
                     [--workload 31b|1b] [--layers L] [--m M] [--no-extras]
+                    [--batch-sweep] [--bf16-lm-head] [--load-time]
 
 One JSON line is printed by rank 0.  With N > 1 (torchrun) every rank runs
 an independent replica on its own GPU (the path has no exchange step).
@@ -73,6 +74,9 @@ def parse():
                         "for m <= 16; the other one is timed among the extras)")
     p.add_argument("--bf16-lm-head", action="store_true",
                    help="time only the bf16 GEMV on the ~31B tied lm_head [262144, 5376], m = 1")
+    p.add_argument("--load-time", action="store_true",
+                   help="time only the load-time kernels (reconstruct + quantise, and "
+                        "quantise alone) on the 1B MLP shapes and the ~31B gate+up")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the eager / no-PDL / end-to-end / CPU-baseline legs")
     return p.parse_args()
@@ -613,6 +617,74 @@ def run_bf16_lm_head(a, dist):
                           "config": {"workload": "~31B tied lm_head, bf16", **r}}), flush=True)
 
 
+def run_load_time(a, dist):
+    """The load-time kernels of the path: theta bundle -> W_eff -> NVFP4
+    (aq_reconstruct_quantize_nvfp4, rank 4) and NVFP4 of a bf16 weight
+    (aq_quantize_nvfp4), on the 1B-shaped MLP weights (fused gate+up
+    [13824, 1152], down [1152, 6912]) and the ~31B fused gate+up [43008,
+    5376].  Each call rotates over enough input copies to exceed L2 twice
+    and is event-timed on the launching stream.  Algorithmic bytes: 2 B read
+    + 0.5625 B written per element + 4 B of g_dec, plus the theta (4 n +
+    2 (n + k) r bytes) for the fused form."""
+    import torch
+    from nvfp4_block_scaled_aq_gb300 import aq, inputs
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(dist.local)
+    device = torch.device("cuda", dist.local)
+    stream = torch.cuda.Stream(device)
+    r = 4
+    shapes = [("1b_gate_up", 13824, 1152), ("1b_down", 1152, 6912), ("31b_gate_up", 43008, 5376)]
+    qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+    rows = []
+    for name, n, k in shapes:
+        copies = max(1, -(-(256 << 20) // (2 * n * k)))
+        thetas = [inputs.theta(n, k, r, seed=inputs.seed_of(9500 + i), device=device)
+                  for i in range(copies)]
+        out = aq.Nvfp4Weight.empty(n, k, device=device)
+        torch.cuda.synchronize()
+        res = {"shape": [n, k], "rank": r, "copies": copies}
+        for form in ("reconstruct_quantize", "quantize"):
+            def call(i):
+                th = thetas[i % copies]
+                if form == "quantize":
+                    aq.quantize(th.W0, out, qws, stream=stream)
+                else:
+                    aq.reconstruct_quantize(th.W0, th.s, th.U, th.V, out, qws, stream=stream)
+            reps = max(2 * copies, 10)
+            with torch.cuda.stream(stream):
+                for i in range(max(a.warmup, copies)):
+                    call(i)
+                stream.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for i in range(reps):
+                    call(i)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            secs = e0.elapsed_time(e1) / 1e3 / reps
+            byts = n * k * 2 + n * k // 2 + n * k // 16 + 4
+            if form == "reconstruct_quantize":
+                byts += 4 * n + 2 * (n + k) * r
+            res[form] = {"us_per_call": round(secs * 1e6, 2), "GBps": round(byts / secs / 1e9, 1),
+                         "algorithmic_bytes": byts}
+        st = aq.poll_device_status()
+        if st != aq.OK:
+            raise RuntimeError("load-time kernels reported %s: %s" % (st, aq.last_error()))
+        rows.append(dict(name=name, **res))
+        del thetas
+    peak, src = load_peaks()
+    if dist.rank == 0:
+        best = max(v["GBps"] for row in rows for k2, v in row.items() if isinstance(v, dict))
+        print(json.dumps({"metric": "load-time reconstruct + NVFP4 quantise, GB/s of algorithmic bytes",
+                          "value": best, "unit": "GB/s", "n_gpus": dist.world, "higher_is_better": True,
+                          "data": "synthetic (seeded theta bundles, N(0, 0.02^2) W0)",
+                          "config": {"workload": "load-time kernels on the 1B MLP and ~31B gate+up shapes",
+                                     "l2": "inputs rotated over copies exceeding 256 MB"},
+                          "hbm_peak_gbs": peak, "hbm_peak_source": src, "shapes": rows}), flush=True)
+
+
 def run_sweep(a, dist):
     """GEMV kernels vs the block-scaled MMA path on the ~31B-shaped fused
     gate+up [43008, 5376] and down [5376, 21504] weights.  Each timing is a
@@ -763,6 +835,8 @@ def main():
             run_sweep(a, dist)
         elif a.bf16_lm_head:
             run_bf16_lm_head(a, dist)
+        elif a.load_time:
+            run_load_time(a, dist)
         else:
             run_aq(a, dist)
     finally:
