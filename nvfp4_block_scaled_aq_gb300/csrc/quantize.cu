@@ -28,7 +28,15 @@ template <int R>
 __device__ __forceinline__ float recon_elem(float w0, float s, const float *u,
                                             const uint16_t *vrow, int r) {
   float delta = 0.0f;
-  if (R >= 0) {
+  if (R == 4) {
+    // the row's four bf16 in one 8-byte load (V is 8-byte aligned whenever
+    // this instantiation is launched)
+    const uint2 vv = __ldg(reinterpret_cast<const uint2 *>(vrow));
+    delta = __fmaf_rn(u[0], bf16_lo(vv.x), delta);
+    delta = __fmaf_rn(u[1], bf16_hi(vv.x), delta);
+    delta = __fmaf_rn(u[2], bf16_lo(vv.y), delta);
+    delta = __fmaf_rn(u[3], bf16_hi(vv.y), delta);
+  } else if (R >= 0) {
 #pragma unroll
     for (int t = 0; t < R; ++t)
       delta = __fmaf_rn(u[t], __uint_as_float(uint32_t(vrow[t]) << 16), delta);
@@ -339,7 +347,7 @@ cudaError_t launch_reconstruct(const uint16_t *W0, const float *s, const uint16_
   const int grid = grid_for(int64_t(n) * (k / 8), kThreads, 152 * 16);
   if (r == 0)
     reconstruct_kernel<0><<<grid, kThreads, 0, st>>>(W0, s, U, V, n, k, r, W_eff);
-  else if (r == 4)
+  else if (r == 4 && (reinterpret_cast<uintptr_t>(V) & 7u) == 0)
     reconstruct_kernel<4><<<grid, kThreads, 0, st>>>(W0, s, U, V, n, k, r, W_eff);
   else
     reconstruct_kernel<-1><<<grid, kThreads, 0, st>>>(W0, s, U, V, n, k, r, W_eff);
@@ -377,7 +385,7 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
     quantize_pass<0, false>(W, s, U, V, 0, n, k, out, amax, dev, st);
   else if (r == 0)
     quantize_pass<0, true>(W, s, U, V, r, n, k, out, amax, dev, st);
-  else if (r == 4)
+  else if (r == 4 && (reinterpret_cast<uintptr_t>(V) & 7u) == 0)
     quantize_pass<4, true>(W, s, U, V, r, n, k, out, amax, dev, st);
   else
     quantize_pass<-1, true>(W, s, U, V, r, n, k, out, amax, dev, st);
