@@ -24,6 +24,7 @@ import argparse
 import hashlib
 import json
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -46,7 +47,7 @@ NCU_TRAFFIC = {
     # one-token kernel form, captured without cache flushing so the L2
     # prefetch of the next projection counts where it is issued: reads
     # 19,086,336 + 15,315,456 + 142,870,272 + 68,184,064, writes 91,136 +
-    # 77,824 + 408,576 + 165,376 (profiles/gemv_kernel_31b_layer_dram_traffic.md);
+    # 77,824 + 408,576 + 165,376 (the committed ncu summary of that capture);
     # the key is of the sources after comment-only edits to gemv.cu, the
     # device code unchanged since the capture
     ("gemma4-31b-shaped decode-step weight stream", 1, "83e96172c032b4ac9ada6f291548c27441508458"): 246199040,
@@ -74,6 +75,8 @@ def parse():
                         "for m <= 16; the other one is timed among the extras)")
     p.add_argument("--bf16-lm-head", action="store_true",
                    help="time only the bf16 GEMV on the ~31B tied lm_head [262144, 5376], m = 1")
+    p.add_argument("--small-configs", action="store_true",
+                   help="1B-shaped single projections (fused QKV, MLP) per call, L2-cold and warm")
     p.add_argument("--load-time", action="store_true",
                    help="time only the load-time kernels (reconstruct + quantise, and "
                         "quantise alone) on the 1B MLP shapes and the ~31B gate+up")
@@ -403,6 +406,87 @@ def epilogue_leg(stream, dist, a, device):
             "kernels": "gemv_kernel<1, plain | low-rank (after vx_kernel) | GLU epilogue>"}
 
 
+def small_gemv_timing(n, k, copies, pdl, stream, dist, a, device):
+    """Microseconds per call of the m = 1 NVFP4 GEMV on [n, k]: a CUDA graph
+    of calls over `copies` seeded weights in turn (one copy: the same weight
+    every call, L2-warm), with or without programmatic dependent launch
+    between the calls; event-timed on the launching stream."""
+    import torch
+    from nvfp4_block_scaled_aq_gb300 import aq, inputs
+    qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+    ws_w = []
+    for c in range(copies):
+        W = inputs.weight(n, k, seed=inputs.seed_of(9700 + c), device=device)
+        w = aq.Nvfp4Weight.empty(n, k, device=device)
+        aq.quantize(W, w, qws)
+        ws_w.append(w)
+        del W
+    x = inputs.tokens(1, k, seed=inputs.seed_of(9701), device=device)
+    y = torch.empty((1, n), dtype=torch.bfloat16, device=device)
+    ws = torch.zeros(aq.gemv_workspace_bytes(n, k, 1), dtype=torch.uint8, device=device)
+    calls = max(copies, 64)
+    flags = aq.STEP_REGDECODE | (aq.STEP_PDL if pdl else 0)
+    args = [aq.StepArgs([w], [x], [y]) for w in ws_w]
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        aq.decode_step(args[0], ws, flags=flags, stream=stream)
+        stream.synchronize()
+        with torch.cuda.graph(gr, stream=stream):
+            for i in range(calls):
+                aq.decode_step(args[i % copies], ws, flags=flags, stream=stream)
+    torch.cuda.synchronize()
+
+    def run():
+        with torch.cuda.stream(stream):
+            gr.replay()
+    reps = max(5, a.steps // 10)
+    secs = time_region(run, reps, a.warmup, stream, dist) / (reps * calls)
+    del gr, ws_w
+    torch.cuda.synchronize()
+    return secs
+
+
+def run_small_configs(a, dist):
+    """The 1B-shaped single projections at m = 1: the fused QKV [1536,
+    1152] and the MLP's fused gate+up [13824, 1152] and down [1152, 6912].
+    Per call: L2-cold (a graph over seeded weight copies that together
+    exceed twice L2, in turn), chained with programmatic dependent launch
+    and stream-ordered without it, and L2-warm (one weight, every call).
+    GB/s of algorithmic bytes (0.5625 B per weight element + 4 + 2k + 2n)."""
+    import torch
+    from nvfp4_block_scaled_aq_gb300 import aq, inputs
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(dist.local)
+    device = torch.device("cuda", dist.local)
+    stream = torch.cuda.Stream(device)
+    peak, src = load_peaks()
+    rows = []
+    for name, (n, k) in (("fused_qkv", inputs.LAYER_1B[0]), ("fused_gate_up", inputs.LAYER_1B[2]),
+                         ("down", inputs.LAYER_1B[3])):
+        byts = n * k // 2 + n * k // 16 + 4 + 2 * k + 2 * n
+        copies = -(-(2 * 129 * 10**6) // (n * k // 2 + n * k // 16))
+        row = {"name": name, "shape": [n, k], "m": 1, "algorithmic_bytes": byts, "cold_copies": copies}
+        for label, cp, pdl in (("cold_pdl", copies, True), ("cold_no_pdl", copies, False),
+                               ("warm_pdl", 1, True)):
+            secs = small_gemv_timing(n, k, cp, pdl, stream, dist, a, device)
+            row[label] = {"us_per_call": round(secs * 1e6, 3), "GBps": round(byts / secs / 1e9, 1),
+                          "frac_of_peak": round(byts / secs / 1e9 / peak, 4)}
+        rows.append(row)
+    st = aq.poll_device_status()
+    if st != aq.OK:
+        raise RuntimeError("device status %d: %s" % (st, aq.last_error()))
+    if dist.rank == 0:
+        print(json.dumps({"metric": "1B-shaped single-projection NVFP4 GEMV, us per call and GB/s",
+                          "value": rows[0]["cold_pdl"]["us_per_call"], "unit": "us per call (fused QKV, cold, PDL)",
+                          "n_gpus": dist.world, "higher_is_better": False,
+                          "data": "synthetic (seeded N(0,0.02^2) weights with 0.1% x20 outliers, N(0,1) tokens)",
+                          "config": {"workload": "1B-shaped fused QKV, gate+up and down at m = 1",
+                                     "l2": "cold legs rotate over weight copies exceeding twice L2"},
+                          "hbm_peak_gbs": peak, "hbm_peak_source": src, "projections": rows}), flush=True)
+
+
 def kernel_sha():
     h = hashlib.sha1()
     for name in ("gemv_core.cuh", "gemv.cu"):
@@ -420,40 +504,97 @@ def load_peaks():
         return 6800.0, "fallback"
 
 
-def cpu_baseline(shapes, m, budget_s=10.0, seed=0):
-    """The oracle's fp64 GEMV, as it stands, on the host: rows of layer 0's
-    projections (seeded like the GPU workload but drawn on the CPU) until
-    the time budget is spent.  Returns GB/s of algorithmic bytes."""
-    import numpy as np
+def host_cpu():
+    """(model name, usable host cores) of the machine the oracle runs on."""
+    model = platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Vendor ID") and ":" in line:
+                model = line.split(":", 1)[1].strip()
+                if line.startswith("Model name"):
+                    break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except AttributeError:
+        cores = os.cpu_count() or 1
+    return model, cores
+
+
+def oracle_rows(shapes, m, seed=0, max_rows=8192):
+    """Layer 0's projections quantised by the oracle (seeded like the GPU
+    workload, drawn on the CPU): (packed, scales, g_dec, x, rows, k) each."""
     import oracle
     from nvfp4_block_scaled_aq_gb300 import inputs
-    done_bytes = 0.0
-    spent = 0.0
-    rows_done = 0
-    per_proj = budget_s / len(shapes)
+    prepared = []
     for p, (n, k) in enumerate(shapes):
-        rows = min(n, 8192)
+        rows = min(n, max_rows)
         W = inputs.bits_u16(inputs.weight(rows, k, seed=inputs.seed_of(seed, 0, p)))
         x = inputs.bits_u16(inputs.tokens(m, k, seed=inputs.seed_of(seed + 1, 0, p)))
         packed, scales, ge, gd = oracle.quantize(W)
-        r0 = 0
-        t_proj = 0.0
-        while r0 < rows and t_proj < per_proj:
-            r1 = min(rows, r0 + 64)
-            sel = np.arange(r0, r1)
-            t = time.perf_counter()
-            oracle.gemv(packed, scales, gd, x, rows=sel)
-            dt = time.perf_counter() - t
-            t_proj += dt
-            done_bytes += (r1 - r0) * (k // 2 + k // 16) + 2 * m * (r1 - r0)
-            rows_done += r1 - r0
-            r0 = r1
-        done_bytes += 2 * m * k + 4
-        spent += t_proj
-    return {"value": done_bytes / spent / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+        prepared.append((packed, scales, gd, x, rows, k))
+    return prepared
+
+
+def oracle_gemv_leg(prepared, m, threads, budget_s):
+    """The oracle's fp64 GEMV, as it stands, over 64-row chunks of the
+    prepared projections (each projection gets an equal share of the time
+    budget), on `threads` host threads at once (ctypes releases the GIL for
+    the C call, so the threads run on separate cores).  Returns (bytes,
+    wall seconds, rows)."""
+    import concurrent.futures as cf
+    import threading
+    import numpy as np
+    import oracle
+    done = [0.0, 0]
+    lock = threading.Lock()
+    wall = 0.0
+    for packed, scales, gd, x, rows, k in prepared:
+        chunks = iter(range(0, rows, 64))
+        deadline = [None]
+
+        def worker():
+            while True:
+                with lock:
+                    if time.perf_counter() > deadline[0]:
+                        return
+                    r0 = next(chunks, None)
+                if r0 is None:
+                    return
+                r1 = min(rows, r0 + 64)
+                oracle.gemv(packed, scales, gd, x, rows=np.arange(r0, r1))
+                with lock:
+                    done[0] += (r1 - r0) * (k // 2 + k // 16) + 2 * m * (r1 - r0)
+                    done[1] += r1 - r0
+        t = time.perf_counter()
+        deadline[0] = t + budget_s / len(prepared)
+        with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+            for f in [ex.submit(worker) for _ in range(threads)]:
+                f.result()
+        wall += time.perf_counter() - t
+        done[0] += 2 * m * k + 4
+    return done[0], wall, done[1]
+
+
+def cpu_baseline(shapes, m, budget_s=12.0, seed=0):
+    """The oracle's fp64 GEMV, as it stands, on the host: rows of layer 0's
+    projections until the time budget is spent, first on one core, then on
+    every host core at once.  Returns GB/s of algorithmic bytes for the
+    all-cores leg, with the one-core leg beside it."""
+    prepared = oracle_rows(shapes, m, seed)
+    model, cores = host_cpu()
+    b1, s1, r1 = oracle_gemv_leg(prepared, m, 1, budget_s / 3)
+    bn, sn, rn = oracle_gemv_leg(prepared, m, cores, budget_s * 2 / 3)
+    total_rows = sum(n for n, _ in shapes)
+    return {"value": bn / sn / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "cpu": model,
             "sample": "%d rows of layer-0 projections (of %d rows x 60 layers), m=%d, "
-                      "fp64 accumulation, single thread" % (rows_done, sum(n for n, _ in shapes), m),
-            "seconds": round(spent, 3)}
+                      "fp64 accumulation, %d threads (one per host core)" % (rn, total_rows, m, cores),
+            "seconds": round(sn, 3),
+            "single_thread": {"value": b1 / s1 / 1e9, "unit": "GB/s", "cores": 1,
+                              "sample": "%d rows" % r1, "seconds": round(s1, 3)}}
 
 
 def run_aq(a, dist):
@@ -778,48 +919,47 @@ def run_sweep(a, dist):
 # ------------------------------------------------------------ reference arm
 
 def run_reference(a, dist):
-    """The CPU oracle as it stands, on the host cores, on a bounded sample
-    of the same workload: each step is the oracle's GEMV over 256 rows of
-    each of layer 0's projections."""
+    """The CPU oracle as it stands, on every host core, on a bounded sample
+    of the same workload: each step is the oracle's GEMV over 64 rows per
+    host core of each of layer 0's projections, one thread per core (ctypes
+    releases the GIL for the C call)."""
     if dist.rank != 0:
         return
+    import concurrent.futures as cf
     import numpy as np
     import oracle
-    from nvfp4_block_scaled_aq_gb300 import inputs
     name, shapes, layers = workload(a.workload)
     m = a.m
-    prepared = []
-    for p, (n, k) in enumerate(shapes):
-        rows = min(n, 64)
-        W = inputs.bits_u16(inputs.weight(rows, k, seed=inputs.seed_of(0, 0, p)))
-        x = inputs.bits_u16(inputs.tokens(m, k, seed=inputs.seed_of(1, 0, p)))
-        packed, scales, ge, gd = oracle.quantize(W)
-        prepared.append((packed, scales, gd, x, rows, k))
+    model, cores = host_cpu()
+    prepared = oracle_rows(shapes, m, max_rows=64 * cores)
     step_bytes = sum(r * (k // 2 + k // 16) + 2 * m * k + 2 * m * r + 4
                      for _, _, _, _, r, k in prepared)
+    jobs = [(packed, scales, gd, x, np.arange(r0, min(rows, r0 + 64)))
+            for packed, scales, gd, x, rows, k in prepared for r0 in range(0, rows, 64)]
+    ex = cf.ThreadPoolExecutor(max_workers=cores)
 
     def step():
-        for packed, scales, gd, x, rows, k in prepared:
-            oracle.gemv(packed, scales, gd, x)
+        list(ex.map(lambda j: oracle.gemv(j[0], j[1], j[2], j[3], rows=j[4]), jobs))
     for _ in range(a.warmup):
         step()
     t = time.perf_counter()
     for _ in range(a.steps):
         step()
     secs = time.perf_counter() - t
+    ex.shutdown()
     value = step_bytes * a.steps / secs / 1e9
-    sample = ("64 rows of each of layer 0's 4 projections per step (%d of %d weight bytes "
-              "of a full step), m=%d, fp64 accumulation" %
-              (sum(r * (k // 2 + k // 16) for _, _, _, _, r, k in prepared),
-               weight_bytes(shapes, layers), m))
+    sample = ("%d rows of each of layer 0's 4 projections per step (%d of %d weight bytes "
+              "of a full step), m=%d, fp64 accumulation, %d threads" %
+              (64 * cores, sum(r * (k // 2 + k // 16) for _, _, _, _, r, k in prepared),
+               weight_bytes(shapes, layers), m, cores))
     out = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
            "n_gpus": dist.world, "steps": a.steps, "warmup": a.warmup,
            "ms_per_step": round(secs / a.steps * 1e3, 3), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 accumulate (CPU oracle)",
            "data": "synthetic (seeded, drawn on the CPU)",
            "config": {"workload": name + " (bounded sample)", "m": m},
-           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
-                            "kind": "oracle", "sample": sample},
+           "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                            "kind": "oracle", "cpu": model, "sample": sample},
            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -837,6 +977,8 @@ def main():
             run_bf16_lm_head(a, dist)
         elif a.load_time:
             run_load_time(a, dist)
+        elif a.small_configs:
+            run_small_configs(a, dist)
         else:
             run_aq(a, dist)
     finally:

@@ -220,18 +220,23 @@ AQ_API aq_status aq_quantize_act_nvfp4(const uint16_t *x, int32_t m, int32_t k,
  * create them.  The pages have no counterpart of this call; it exists for
  * such callers only.
  *
- * Arguments, results and errors are those of aq_gemv_nvfp4, computed by
- * the register-decode kernel whatever m is: outputs equal aq_gemv_nvfp4
- * with AQ_PATH_GEMV_REGDECODE bit for bit (AQ_PATH_GEMV_TCGEN05 is
- * rejected with AQ_ERR_UNSUPPORTED).  The split-K
+ * Arguments, results and errors are those of aq_gemv_nvfp4 on the
+ * register-decode kernel, which computes every call: 1 <= m <= AQ_MAX_M,
+ * and outputs equal aq_gemv_nvfp4 with AQ_PATH_GEMV_REGDECODE bit for bit.
+ * AQ_PATH_MMA, AQ_PATH_GEMV_TCGEN05, and AQ_PATH_AUTO with m > AQ_MAX_M
+ * (where aq_gemv_nvfp4 would take the MMA path) are rejected with
+ * AQ_ERR_UNSUPPORTED.  The split-K
  * scratch is a fixed array of AQ_GEMV_NOALLOC_MAX_SCRATCH bytes inside the
  * library, in device memory, which every GPU that loads the library holds
  * until the process exits; nothing is allocated, on the device or the host.
- * A weight whose scratch (aq_gemv_workspace_bytes(n, k, m) on the current
- * device) exceeds that size is rejected with AQ_ERR_WORKSPACE before any
- * launch.  The first call on each device sets the array up synchronously
- * (looks up its address and zero-fills it), so that first call must come
- * before any stream capture.  Every call then clears, on `stream`, the
+ * A weight whose register-decode scratch on the current device exceeds that
+ * size is rejected with AQ_ERR_WORKSPACE before any launch (that scratch
+ * is 12 MiB plus 8 KiB x the number of 128-row blocks x the most CTAs that
+ * share one of them, and never more than aq_gemv_workspace_bytes(n, k, m)).  The first call on each device
+ * sets the array up synchronously (looks up its address and zero-fills
+ * it), so that first call must come before any stream capture; the address
+ * is kept for the life of the process, so the call must not be used across
+ * a cudaDeviceReset.  Every call then clears, on `stream`, the
  * part of the array that has to start at zero, and launches the GEMV.
  * All calls on a device share the one array, which keeps the last call's
  * contents: calls whose kernels can overlap on the GPU (different streams,

@@ -214,8 +214,15 @@ struct GemvPlan {
 // Split-K tickets per row block at the start of a GEMV workspace (one per
 // 16-row group of the register-decode kernel).
 constexpr int kTicketsPerRowBlock = 8;
-GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev);
+// Row groups of 16 rows per CTA of the register-decode GEMV (the single
+// calls and the decode step): 8 (two CTAs per SM, 128-row units) or 16 (one
+// CTA per SM, 256-row units).  Measured on the ~31B step at m = 1: 3.26 ms
+// with 8, 3.30 ms with 16 (per-projection launches); the persistent step
+// 3.80 / 3.77 ms.
+constexpr int kGemvRG = 8;
+GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev, int rg);
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev);
+size_t gemv_regdecode_workspace_bytes(int n, int k, const DeviceInfo &dev);
 // `next`, when given, is the projection launched after this one on the same
 // stream: the kernel prefetches the first weight units of it into L2.
 cudaError_t launch_gemv(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint16_t *y,

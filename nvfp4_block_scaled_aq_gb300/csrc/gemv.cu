@@ -65,14 +65,14 @@ using namespace core;
 
 namespace {
 
-template <int NT, int EPI, bool BD = false>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+template <int NT, int EPI, bool BD, int RG>
+__global__ void __launch_bounds__(Geo<RG>::kThreads, Geo<RG>::kCtasPerSm)
     gemv_kernel(const __grid_constant__ CUtensorMap tm_w,
                 const __grid_constant__ CUtensorMap tm_s,
                 const __grid_constant__ CUtensorMap tm_nw,
                 const __grid_constant__ CUtensorMap tm_ns, Proj p, const Run r) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const SmemView sv = carve(smem_raw, r.stages);
+  const SmemView sv = carve<RG>(smem_raw, r.stages);
   Ctrl &ct = *sv.ct;
   volatile int *aborted = &ct.aborted;
   p.tm_w = &tm_w;
@@ -80,24 +80,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   p.nx_w = &tm_nw;
   p.nx_s = &tm_ns;
   if (threadIdx.x == 0) {
-    init_ring(ct, r.stages);
+    init_ring<RG>(ct, r.stages);
     pdl_launch_dependents();
   }
   __syncthreads();
   RingPos pos;
-  if ((threadIdx.x >> 5) == kW) {  // producer warp
+  if ((threadIdx.x >> 5) == Geo<RG>::kW) {  // producer warp
     if ((threadIdx.x & 31) == 0) {
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_w)) : "memory");
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tm_s)) : "memory");
-      if (produce(p, sv.base, ct, r.stages, pos, aborted, r.status)) prefetch_next(p);
+      if (produce<RG>(p, sv.base, ct, r.stages, pos, aborted, r.status)) prefetch_next<RG>(p);
       drain(ct, r.stages, pos.count);
     }
     return;
   }
-  prefetch_x_l2(p, r.m);
+  prefetch_x_l2<RG>(p, r.m);
   // x and the workspace may come from the previous kernel: consume() waits
   // for it once its own index work is done
-  consume<NT, EPI, BD>(p, r, sv.base, ct, sv.xs, pos, aborted, true);
+  Dep dep;
+  dep.kind = kDepPdl;
+  consume<NT, EPI, BD, RG>(p, r, sv.base, ct, sv.xs, pos, aborted, dep);
 }
 
 // The kernels' bounded ring wait run against an mbarrier that nothing
@@ -185,35 +187,47 @@ bool cached_map(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows
   return true;
 }
 
-template <int NT, int EPI, bool BD = false>
+template <int NT, int EPI, bool BD, int RG>
 cudaError_t set_smem_attr(int device) {
   static bool done[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, EPI, BD>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+  cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, EPI, BD, RG>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Geo<RG>::kSmemBudget);
   if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
   return e;
 }
 
-// One token: the block-diagonal instantiation of the epilogue kind.
-template <int EPI>
-cudaError_t launch_bd(const cudaLaunchConfig_t &cfg, const CUtensorMap &tm_w,
-                      const CUtensorMap &tm_s, const CUtensorMap &tm_nw, const CUtensorMap &tm_ns,
-                      const Proj &p, const Run &r, int device) {
-  cudaError_t e = set_smem_attr<1, EPI, true>(device);
+template <int NT, int EPI, bool BD, int RG>
+cudaError_t launch_form(const cudaLaunchConfig_t &cfg, const CUtensorMap &tm_w,
+                        const CUtensorMap &tm_s, const CUtensorMap &tm_nw, const CUtensorMap &tm_ns,
+                        const Proj &p, const Run &r, int device) {
+  cudaError_t e = set_smem_attr<NT, EPI, BD, RG>(device);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, gemv_kernel<1, EPI, true>, tm_w, tm_s, tm_nw, tm_ns, p, r);
+  return cudaLaunchKernelEx(&cfg, gemv_kernel<NT, EPI, BD, RG>, tm_w, tm_s, tm_nw, tm_ns, p, r);
 }
-cudaError_t launch_one_token(const cudaLaunchConfig_t &cfg, int epi, const CUtensorMap &tm_w,
-                             const CUtensorMap &tm_s, const CUtensorMap &tm_nw,
-                             const CUtensorMap &tm_ns, const Proj &p, const Run &r, int device) {
+
+// The instantiation for m tokens and the epilogue kind: the block-diagonal
+// form for one token, one n8 block of tokens up to 8, two up to 16.
+template <int EPI, int RG>
+cudaError_t launch_epi(const cudaLaunchConfig_t &cfg, int m, const CUtensorMap &tm_w,
+                       const CUtensorMap &tm_s, const CUtensorMap &tm_nw, const CUtensorMap &tm_ns,
+                       const Proj &p, const Run &r, int device) {
+  if (m == 1) return launch_form<1, EPI, true, RG>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+  if (m <= 8) return launch_form<1, EPI, false, RG>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+  return launch_form<2, EPI, false, RG>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+}
+template <int RG>
+cudaError_t launch_any(const cudaLaunchConfig_t &cfg, int epi, int m, const CUtensorMap &tm_w,
+                       const CUtensorMap &tm_s, const CUtensorMap &tm_nw, const CUtensorMap &tm_ns,
+                       const Proj &p, const Run &r, int device) {
   switch (epi) {
-    case kEpiLowRank: return launch_bd<kEpiLowRank>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
-    case kEpiGlu: return launch_bd<kEpiGlu>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
-    case kEpiSegments: return launch_bd<kEpiSegments>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
-    default: return launch_bd<kEpiPlain>(cfg, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+    case kEpiLowRank: return launch_epi<kEpiLowRank, RG>(cfg, m, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+    case kEpiGlu: return launch_epi<kEpiGlu, RG>(cfg, m, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+    case kEpiSegments: return launch_epi<kEpiSegments, RG>(cfg, m, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
+    default: return launch_epi<kEpiPlain, RG>(cfg, m, tm_w, tm_s, tm_nw, tm_ns, p, r, device);
   }
 }
 
@@ -229,22 +243,28 @@ int x_cap_for(const GemvPlan &p, int m) {
 
 namespace core {
 
-size_t smem_bytes(int stages, int x_cap_halves) {
-  return 1024 + size_t(stages) * kStageBytes + kCtrlBytes + size_t(x_cap_halves) * 2;
+size_t smem_bytes(int stages, int x_cap_halves, int rg) {
+  const int stage = rg == 16 ? Geo<16>::kStageBytes : Geo<8>::kStageBytes;
+  return 1024 + size_t(stages) * stage + kCtrlBytes + size_t(x_cap_halves) * 2;
 }
 
-int stages_for(int x_cap_halves) {
-  const int64_t room = int64_t(kSmemBudget) - 1024 - kCtrlBytes - int64_t(x_cap_halves) * 2;
-  const int64_t st = room / kStageBytes;
-  return int(st > kMaxStages ? kMaxStages : (st < 0 ? 0 : st));
+int stages_for(int x_cap_halves, int rg) {
+  const int budget = rg == 16 ? Geo<16>::kSmemBudget : Geo<8>::kSmemBudget;
+  const int stage = rg == 16 ? Geo<16>::kStageBytes : Geo<8>::kStageBytes;
+  const int most = rg == 16 ? Geo<16>::kMaxStages : Geo<8>::kMaxStages;
+  const int64_t room = int64_t(budget) - 1024 - kCtrlBytes - int64_t(x_cap_halves) * 2;
+  const int64_t st = room / stage;
+  return int(st > most ? most : (st < 0 ? 0 : st));
 }
 
-bool encode_maps(const aq_nvfp4_weight &w, CUtensorMap *tm_w, CUtensorMap *tm_s) {
+// Boxes of 16 rg rows of packed nibbles (128 bytes wide) and rg rows of
+// scale tiles (256 bytes: the unit's two 128-column tiles).
+bool encode_maps(const aq_nvfp4_weight &w, CUtensorMap *tm_w, CUtensorMap *tm_s, int rg) {
   if (!encoder()) return false;
-  if (!cached_map(tm_w, w.packed, uint64_t(w.k) / 2, uint64_t(w.n), kUnitCols, kRB, true))
+  if (!cached_map(tm_w, w.packed, uint64_t(w.k) / 2, uint64_t(w.n), kUnitCols, 16 * rg, true))
     return false;
   const uint64_t srow = uint64_t(ceil_div(w.k, kTileCols)) * 128;
-  return cached_map(tm_s, w.scales, srow, uint64_t(ceil_div(w.n, kTileRows)), kKT * 128, kRG,
+  return cached_map(tm_s, w.scales, srow, uint64_t(ceil_div(w.n, kTileRows)), kKT * 128, rg,
                     false);
 }
 
@@ -271,9 +291,9 @@ bool encode_act_maps(const uint8_t *xq, const uint8_t *xs, int m, int k, int sca
                   CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev) {
+GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev, int rg) {
   GemvPlan p;
-  p.row_blocks = ceil_div(n, kRB);
+  p.row_blocks = ceil_div(n, 16 * rg);
   p.k_tiles = ceil_div(k, kTileCols);
   p.units = ceil_div(p.k_tiles, kKT);
   p.total = p.row_blocks * p.units;
@@ -284,7 +304,7 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev) {
   // no CTA idles while others finish an extra unit, and fewer CTAs share
   // each split row block.  The grid depends only on (n, k) and the SM
   // count, never on m.
-  int64_t g = int64_t(dev.sms) * kCtasPerSm;
+  int64_t g = int64_t(dev.sms) * (rg == 8 ? Geo<8>::kCtasPerSm : Geo<16>::kCtasPerSm);
   if (g > p.total) g = p.total;
   if (g < 1) g = 1;
   const int64_t longest = (p.total + g - 1) / g;
@@ -300,10 +320,16 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev) {
   return p;
 }
 
+// The register-decode kernel's own need: tickets, the zero region, and
+// fp32 partials [row_blocks][max_contrib][kRB][16 tokens].
+size_t gemv_regdecode_workspace_bytes(int n, int k, const DeviceInfo &dev) {
+  const GemvPlan p = plan_gemv(n, k, dev, kGemvRG);
+  return kRestOffset + size_t(p.row_blocks) * p.max_contrib * (16 * kGemvRG) * 16 * sizeof(float);
+}
+
 // Enough for either kernel, so one workspace serves every token count.
 size_t gemv_workspace_bytes(int n, int k, const DeviceInfo &dev) {
-  const GemvPlan p = plan_gemv(n, k, dev);
-  const size_t reg = kRestOffset + size_t(p.row_blocks) * p.max_contrib * kRB * 16 * sizeof(float);
+  const size_t reg = gemv_regdecode_workspace_bytes(n, k, dev);
   const size_t tc = gemv_tc_workspace_bytes(n, k, dev);
   return reg > tc ? reg : tc;
 }
@@ -325,9 +351,10 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
                                   cudaStream_t st, const aq_nvfp4_weight *next,
                                   const LowRank *lr, bool glu, int nseg,
                                   const int32_t *seg_end) {
-  const GemvPlan plan = plan_gemv(w.n, w.k, dev);
+  constexpr int RG = kGemvRG;
+  const GemvPlan plan = plan_gemv(w.n, w.k, dev, RG);
   CUtensorMap tm_w, tm_s, tm_nw, tm_ns;
-  if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
+  if (!encode_maps(w, &tm_w, &tm_s, RG)) return cudaErrorInvalidValue;
 
   Run r{};
   uint8_t *wsb = static_cast<uint8_t *>(ws);
@@ -337,7 +364,7 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   r.status = dev.status;
   r.m = m;
   r.x_cap = x_cap_for(plan, m);
-  r.stages = stages_for(r.x_cap);
+  r.stages = stages_for(r.x_cap, RG);
   if (r.stages < kMinStages) return cudaErrorInvalidConfiguration;
 
   Proj p{};
@@ -352,7 +379,7 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   p.units = int(plan.units);
   p.max_contrib = plan.max_contrib;
   p.grid = plan.grid;
-  p.direct = direct_partials_fit(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
+  p.direct = direct_partials_fit<RG>(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
   p.scale_box = 1;
   if (nseg > 0) {
     p.nseg = nseg;
@@ -368,8 +395,8 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
   p.nx_total = 0;
   p.nx_units = p.nx_grid = p.nx_pf = 0;
   if (next) {
-    if (!encode_maps(*next, &tm_nw, &tm_ns)) return cudaErrorInvalidValue;
-    const GemvPlan np = plan_gemv(next->n, next->k, dev);
+    if (!encode_maps(*next, &tm_nw, &tm_ns, RG)) return cudaErrorInvalidValue;
+    const GemvPlan np = plan_gemv(next->n, next->k, dev, RG);
     p.nx_total = np.total;
     p.nx_units = int(np.units);
     p.nx_grid = np.grid;
@@ -381,43 +408,16 @@ cudaError_t launch_gemv_regdecode(const aq_nvfp4_weight &w, const uint16_t *x, i
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes(r.stages, r.x_cap);
+  cfg.blockDim = dim3(Geo<RG>::kThreads);
+  cfg.dynamicSmemBytes = smem_bytes(r.stages, r.x_cap, RG);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  cudaError_t e;
   const int epi = glu ? kEpiGlu : lr ? kEpiLowRank : nseg > 0 ? kEpiSegments : kEpiPlain;
-  if (m == 1) return launch_one_token(cfg, epi, tm_w, tm_s, tm_nw, tm_ns, p, r, dev.ordinal);
-  if (m <= 8 && epi == kEpiPlain) {
-    if ((e = set_smem_attr<1, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiPlain>, tm_w, tm_s, tm_nw, tm_ns, p, r);
-  } else if (epi == kEpiPlain) {
-    if ((e = set_smem_attr<2, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiPlain>, tm_w, tm_s, tm_nw, tm_ns, p, r);
-  } else if (m <= 8 && epi == kEpiLowRank) {
-    if ((e = set_smem_attr<1, kEpiLowRank>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiLowRank>, tm_w, tm_s, tm_nw, tm_ns, p, r);
-  } else if (epi == kEpiLowRank) {
-    if ((e = set_smem_attr<2, kEpiLowRank>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiLowRank>, tm_w, tm_s, tm_nw, tm_ns, p, r);
-  } else if (m <= 8 && epi == kEpiSegments) {
-    if ((e = set_smem_attr<1, kEpiSegments>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiSegments>, tm_w, tm_s, tm_nw, tm_ns, p, r);
-  } else if (epi == kEpiSegments) {
-    if ((e = set_smem_attr<2, kEpiSegments>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiSegments>, tm_w, tm_s, tm_nw, tm_ns, p, r);
-  } else if (m <= 8) {
-    if ((e = set_smem_attr<1, kEpiGlu>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiGlu>, tm_w, tm_s, tm_nw, tm_ns, p, r);
-  } else {
-    if ((e = set_smem_attr<2, kEpiGlu>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiGlu>, tm_w, tm_s, tm_nw, tm_ns, p, r);
-  }
-  return e;
+  return launch_any<RG>(cfg, epi, m, tm_w, tm_s, tm_nw, tm_ns, p, r, dev.ordinal);
 }
 
 cudaError_t launch_selftest_wait(unsigned polls, const DeviceInfo &dev, cudaStream_t st) {
@@ -431,13 +431,14 @@ cudaError_t launch_selftest_wait(unsigned polls, const DeviceInfo &dev, cudaStre
 cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, int m,
                                  uint16_t *y, void *ws, const DeviceInfo &dev,
                                  cudaStream_t st) {
-  const GemvPlan plan = plan_gemv(w.n, w.k, dev);
+  constexpr int RG = kGemvRG;
+  const GemvPlan plan = plan_gemv(w.n, w.k, dev, RG);
   CUtensorMap tm_w, tm_s;
   if (!encoder()) return cudaErrorInvalidValue;
-  if (!make_map(&tm_w, w.packed, uint64_t(w.k) / 2, uint64_t(w.n), kUnitCols, kRB, true))
+  if (!make_map(&tm_w, w.packed, uint64_t(w.k) / 2, uint64_t(w.n), kUnitCols, 16 * RG, true))
     return cudaErrorInvalidValue;
   const uint64_t srow = uint64_t(ceil_div(w.k, kTileCols)) * 128;
-  if (!make_map(&tm_s, w.scales, srow, uint64_t(ceil_div(w.n, kTileRows)), kKT * 128, kRG, false))
+  if (!make_map(&tm_s, w.scales, srow, uint64_t(ceil_div(w.n, kTileRows)), kKT * 128, RG, false))
     return cudaErrorInvalidValue;
 
   Run r{};
@@ -448,7 +449,7 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   r.status = dev.status;
   r.m = m;
   r.x_cap = x_cap_for(plan, m);
-  r.stages = stages_for(r.x_cap);
+  r.stages = stages_for(r.x_cap, RG);
   if (r.stages < kMinStages) return cudaErrorInvalidConfiguration;
 
   Proj p{};
@@ -463,7 +464,7 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
   p.units = int(plan.units);
   p.max_contrib = plan.max_contrib;
   p.grid = plan.grid;
-  p.direct = direct_partials_fit(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
+  p.direct = direct_partials_fit<RG>(plan.row_blocks, plan.max_contrib, m) ? 1 : 0;
   p.scale_box = 1;
   p.nx_w = p.nx_s = nullptr;  // no prefetch of a next projection
   p.nx_total = 0;
@@ -471,19 +472,10 @@ cudaError_t launch_gemv_uncached(const aq_nvfp4_weight &w, const uint16_t *x, in
 
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes(r.stages, r.x_cap);
+  cfg.blockDim = dim3(Geo<RG>::kThreads);
+  cfg.dynamicSmemBytes = smem_bytes(r.stages, r.x_cap, RG);
   cfg.stream = st;
-  cudaError_t e;
-  if (m == 1) return launch_one_token(cfg, kEpiPlain, tm_w, tm_s, tm_w, tm_s, p, r, dev.ordinal);
-  if (m <= 8) {
-    if ((e = set_smem_attr<1, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<1, kEpiPlain>, tm_w, tm_s, tm_w, tm_s, p, r);
-  } else {
-    if ((e = set_smem_attr<2, kEpiPlain>(dev.ordinal)) != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, gemv_kernel<2, kEpiPlain>, tm_w, tm_s, tm_w, tm_s, p, r);
-  }
-  return e;
+  return launch_any<RG>(cfg, kEpiPlain, m, tm_w, tm_s, tm_w, tm_s, p, r, dev.ordinal);
 }
 
 }  // namespace aq

@@ -244,7 +244,7 @@ cudaError_t launch_gemv_bf16(const uint16_t *w, int n, int k, const uint16_t *x,
   r.status = dev.status;
   r.m = m;
   r.x_cap = bf16_x_cap(plan, m);
-  r.stages = stages_for(r.x_cap);
+  r.stages = stages_for(r.x_cap, 8);
   if (r.stages < kMinStages) return cudaErrorInvalidConfiguration;
 
   Proj p{};
@@ -262,7 +262,7 @@ cudaError_t launch_gemv_bf16(const uint16_t *w, int n, int k, const uint16_t *x,
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(plan.grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem_bytes(r.stages, r.x_cap);
+  cfg.dynamicSmemBytes = smem_bytes(r.stages, r.x_cap, 8);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

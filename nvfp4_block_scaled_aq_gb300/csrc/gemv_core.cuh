@@ -49,6 +49,33 @@ constexpr size_t kZeroBytes = size_t(8) << 20;
 constexpr size_t kRestOffset = kTicketBytes + kZeroBytes;
 static_assert(kTicketsPerRowBlock == kRG, "one ticket per row group");
 static_assert(kStageBytes % 1024 == 0, "128-byte swizzle needs 1 KiB-aligned stages");
+
+// Geometry of the register-decode kernels for RG row groups (consumer warps)
+// per CTA.  RG = 8: 128-row units of 18 KiB, two CTAs per SM (the constants
+// above).  RG = 16: 256-row units of 36 KiB, one CTA per SM with sixteen
+// consumer warps and one producer warp on one shared ring -- the SM's
+// warps then finish a projection together (two CTAs on an SM do not: the
+// warp schedulers favour the older one), the SM stages the activations
+// once, and one 2-D copy moves 32 KiB.  Ticket words: RG per row block of
+// 16 RG rows, so kTicketBytes serves both.
+template <int RG>
+struct Geo {
+  static constexpr int kRG = RG;
+  static constexpr int kRB = 16 * RG;
+  static constexpr int kW = RG;
+  static constexpr int kThreads = (RG + 1) * 32;
+  static constexpr int kCtasPerSm = RG == 8 ? 2 : 1;
+  static constexpr int kPackedStage = kRB * kUnitCols;
+  static constexpr int kScaleStage = RG * 128 * kKT;
+  static constexpr int kStageBytes = kPackedStage + kScaleStage;
+  static constexpr int kSmemBudget = RG == 8 ? 113 * 1024 : 227 * 1024;
+  // Deeper rings stream HBM more slowly (measured with these boxes: two
+  // CTAs per SM peak at 3-4 stages of 18 KiB, one CTA per SM at 4 of 36 KiB).
+  static constexpr int kMaxStages = RG == 8 ? 6 : 4;
+  static_assert(RG == 8 || RG == 16, "8 or 16 row groups");
+  static_assert(kStageBytes % 1024 == 0, "128-byte swizzle needs 1 KiB-aligned stages");
+  static_assert(kMaxStages <= 6, "Ctrl holds six barrier pairs");
+};
 static_assert(kUnitCols == 128, "the swizzle pattern assumes 128-byte rows");
 
 // Control block that follows the ring in shared memory.
@@ -56,7 +83,7 @@ struct Ctrl {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
   uint4 zero;               // 16 zero bytes: B operand of the one-token form
-  uint32_t xmax[16];
+  uint32_t xmax[32];       // per token, or per (token, warp) for m <= 2
   int shift[16];
   int flag;
   int aborted;
@@ -121,14 +148,15 @@ struct Proj {
 
 // The reducer of a split row block can poll the partials themselves when
 // they are stored encoded in the zero region: [row_blocks][max_contrib - 1]
-// [m][kRB] words of ~bits(partial) (never zero: no fp32 operation yields
+// [m][rows per row block] words of ~bits(partial) (never zero: no fp32 operation yields
 // the all-ones NaN), which it reads, adds and puts back to zero.  Used for
 // m <= 8 (the one-n8-block kernel, where its registers are free) when the
 // words fit the region; the sums are the same either way.
+template <int RG = 8>
 __host__ __device__ __forceinline__ bool direct_partials_fit(int64_t row_blocks, int max_contrib,
                                                              int m) {
   return m <= 8 && max_contrib <= 16 &&
-         size_t(row_blocks) * size_t(max_contrib - 1) * size_t(m) * kRB * 4 <= kZeroBytes;
+         size_t(row_blocks) * size_t(max_contrib - 1) * size_t(m) * Geo<RG>::kRB * 4 <= kZeroBytes;
 }
 
 // Units of the next projection each CTA prefetches into L2 once its own
@@ -290,8 +318,54 @@ __device__ __forceinline__ uint64_t l2_evict_first_policy() {
 }
 
 // Consumer-warps-only barrier (the producer warp never joins it).
+template <int RG = 8>
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kW * 32) : "memory");
+  asm volatile("bar.sync 1, %0;" ::"n"(Geo<RG>::kW * 32) : "memory");
+}
+
+// What the consumers wait for before they read x (the weights never wait):
+// nothing, the previous kernel on the stream (programmatic dependent
+// launch), or, inside one persistent launch, a completion counter that
+// every CTA of the previous projection bumps once its outputs are written.
+struct Dep {
+  int kind = 0;                  // kDepNone, kDepPdl or kDepCounter
+  const unsigned *ctr = nullptr;
+  unsigned target = 0;           // CTAs of the previous projection
+};
+constexpr int kDepNone = 0;
+constexpr int kDepPdl = 1;
+constexpr int kDepCounter = 2;
+
+// Consumer thread 0 polls the counter (acquire, bounded) until it reaches
+// the target; the barrier then releases every consumer thread after it.
+template <int RG = 8>
+__device__ __forceinline__ void wait_counter(const Dep &d, volatile int *aborted,
+                                             unsigned *status) {
+  if (threadIdx.x == 0) {
+    for (unsigned it = 0;; ++it) {
+      unsigned v;
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(d.ctr) : "memory");
+      if (v >= d.target) break;
+      if (it >= kSpinLimit || *aborted) {
+        if (!*aborted) {
+          *aborted = 1;
+          raise_status(status, kDevTimeout);
+        }
+        break;
+      }
+      __nanosleep(20);
+    }
+  }
+  consumer_sync<RG>();
+}
+
+// Every consumer's writes of a projection precede one release-add by
+// consumer thread 0 (the barrier orders them; release is cumulative).
+template <int RG = 8>
+__device__ __forceinline__ void arrive_counter(unsigned *ctr) {
+  consumer_sync<RG>();
+  if (threadIdx.x == 0)
+    asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
 }
 
 // v * 2^e exactly (two steps keep each factor a normal fp32).
@@ -468,6 +542,7 @@ __device__ __forceinline__ void unit_mma(float (&acc)[2][NT][4], const uint4 (&w
 // numbers the units this CTA handles across every projection of the launch,
 // in the same order the consumers take them.  Returns false after a
 // bounded wait gave up (the CTA is then aborting).
+template <int RG = 8>
 __device__ __forceinline__ bool produce(const Proj &p, uint8_t *base, Ctrl &ct, int S,
                                         RingPos &pos, volatile int *aborted, unsigned *status) {
   const int64_t grid = p.grid;
@@ -488,11 +563,11 @@ __device__ __forceinline__ bool produce(const Proj &p, uint8_t *base, Ctrl &ct, 
       return false;
     }
     if (*aborted) return false;
-    uint8_t *stage = base + st * kStageBytes;
-    mbar_expect_tx(&ct.full[st], p.scale_box ? kStageBytes : kPackedStage);
-    tma_load_2d_hint(stage, p.tm_w, uk * kUnitCols, int(rb * kRB), &ct.full[st], policy);
+    uint8_t *stage = base + st * Geo<RG>::kStageBytes;
+    mbar_expect_tx(&ct.full[st], p.scale_box ? Geo<RG>::kStageBytes : Geo<RG>::kPackedStage);
+    tma_load_2d_hint(stage, p.tm_w, uk * kUnitCols, int(rb * Geo<RG>::kRB), &ct.full[st], policy);
     if (p.scale_box)
-      tma_load_2d_hint(stage + kPackedStage, p.tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[st],
+      tma_load_2d_hint(stage + Geo<RG>::kPackedStage, p.tm_s, uk * kKT * 128, int(rb * Geo<RG>::kRG), &ct.full[st],
                        policy);
     if (++uk == p.units) {
       uk = 0;
@@ -506,6 +581,7 @@ __device__ __forceinline__ bool produce(const Proj &p, uint8_t *base, Ctrl &ct, 
 // this index will load (same partition rule as produce()).  Weights never
 // depend on earlier results, so this may run at any time; it reads nothing
 // into the computation.  Issued by the producer lane after its own loads.
+template <int RG = 8>
 __device__ __forceinline__ void prefetch_next(const Proj &p) {
   if (p.nx_pf <= 0 || int64_t(blockIdx.x) >= p.nx_grid) return;
   const int64_t u_begin = range_begin(blockIdx.x, p.nx_total, p.nx_grid);
@@ -516,11 +592,11 @@ __device__ __forceinline__ void prefetch_next(const Proj &p) {
     const int uk = int(u - rb * p.nx_units);
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(p.nx_w)),
-                 "r"(uk * kUnitCols), "r"(int(rb * kRB))
+                 "r"(uk * kUnitCols), "r"(int(rb * Geo<RG>::kRB))
                  : "memory");
     asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
                      reinterpret_cast<uint64_t>(p.nx_s)),
-                 "r"(uk * kKT * 128), "r"(int(rb * kRG))
+                 "r"(uk * kKT * 128), "r"(int(rb * Geo<RG>::kRG))
                  : "memory");
   }
 }
@@ -538,6 +614,7 @@ __device__ __forceinline__ void drain(Ctrl &ct, int S, int64_t issued) {
 // for the previous kernel (or projection): a prefetch reads nothing into the
 // computation, and L2 stays coherent with any later write to x, so it is
 // safe before the wait and takes the HBM latency off the staging after it.
+template <int RG = 8>
 __device__ __forceinline__ void prefetch_x_l2(const Proj &p, int m) {
   const int64_t grid = p.grid;
   if (int64_t(blockIdx.x) >= grid) return;
@@ -550,7 +627,7 @@ __device__ __forceinline__ void prefetch_x_l2(const Proj &p, int m) {
   const int uk_begin = int(u_begin % units);
   const int slots = x_slots(L, units);
   const int lines = m * slots * 4;  // 128-byte lines (64 bf16) per 256-column slot
-  for (int i = threadIdx.x; i < lines; i += kW * 32) {
+  for (int i = threadIdx.x; i < lines; i += Geo<RG>::kW * 32) {
     const int tok = i / (slots * 4), rem = i - tok * slots * 4;
     const int s = rem >> 2, q = rem & 3;
     const int uk = all_units ? s : (uk_begin + s) % units;
@@ -570,7 +647,7 @@ __device__ __forceinline__ void prefetch_x_l2(const Proj &p, int m) {
 // contributor waits.
 // contrib / jj: the CTAs sharing the row block and this CTA's index among
 // them, when the caller has them already (contrib == 0: work them out).
-template <int NT, int EPI = kEpiPlain>
+template <int NT, int EPI = kEpiPlain, int RG = 8>
 __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t rb, bool complete,
                                             const float (&vown)[NT][4], float gd, int rg, int sg,
                                             int lane, volatile int *aborted, int contrib = 0,
@@ -585,7 +662,7 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
   //    (bounded) for the count, reads the partials and clears the count.
   const bool reducer = !complete && jj == 0;
   const bool direct = NT == 1 && p.direct;
-  const int64_t zrow = (rb * (p.max_contrib - 1) - 1) * m;  // + (j * m + token) * kRB + row
+  const int64_t zrow = (rb * (p.max_contrib - 1) - 1) * m;  // + (j * m + token) * rows + row
   float fin[NT][4];  // final values before rounding (GLU: stored in pairs at the end)
   bool have = complete;
 #pragma unroll
@@ -594,7 +671,7 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
     for (int i = 0; i < 4; ++i) {
       const int token = nt * 8 + 2 * c + (i & 1);
       const int row_local = rg * 16 + sg + 8 * (i >> 1);
-      const int64_t row = rb * kRB + row_local;
+      const int64_t row = rb * Geo<RG>::kRB + row_local;
       const float v = vown[nt][i];
       if (token >= m || row >= p.n) continue;
       if (complete) {
@@ -605,41 +682,47 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
       } else if (!reducer) {
         if (direct)
           asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(
-                           r.zero + (zrow + int64_t(jj) * m + token) * kRB + row_local),
+                           r.zero + (zrow + int64_t(jj) * m + token) * Geo<RG>::kRB + row_local),
                        "r"(~__float_as_uint(v))
                        : "memory");
         else
-          r.partial[((rb * p.max_contrib + jj) * kRB + row_local) * 16 + token] = v;
+          r.partial[((rb * p.max_contrib + jj) * Geo<RG>::kRB + row_local) * 16 + token] = v;
       }
     }
   if (!complete && !reducer && !direct) {
     __syncwarp();  // the warp's partial stores precede lane 0's release
     if (lane == 0)
-      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(r.tickets + rb * kRG + rg)
+      asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(r.tickets + rb * Geo<RG>::kRG + rg)
                    : "memory");
   } else if (reducer && direct) {
+    // Rows sg and sg + 8 of one token: every other contributor's word of
+    // both is loaded before any is used, so one round trip serves the pair
+    // when the partials are there already.
     bool ok = true;
+    const int64_t qs = int64_t(m) * Geo<RG>::kRB;  // word of contributor q: at + q * qs
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int token = nt * 8 + 2 * c + (i & 1);
-        const int row_local = rg * 16 + sg + 8 * (i >> 1);
-        const int64_t row = rb * kRB + row_local;
-        if (!ok || token >= m || row >= p.n) continue;
-        const int64_t at = (zrow + token) * kRB + row_local;  // word of contributor j: at + j * qs
-        const int64_t qs = int64_t(m) * kRB;
-        uint32_t w[16];
+      for (int b = 0; b < 2; ++b) {
+        const int token = nt * 8 + 2 * c + b;
+        if (!ok || token >= m) continue;
+        const int rl0 = rg * 16 + sg, rl1 = rl0 + 8;
+        const bool v0 = rb * Geo<RG>::kRB + rl0 < p.n, v1 = rb * Geo<RG>::kRB + rl1 < p.n;
+        const int64_t at0 = (zrow + token) * Geo<RG>::kRB + rl0, at1 = at0 + 8;
+        uint32_t w0[16], w1[16];
 #pragma unroll
         for (int q = 1; q < 16; ++q) {
-          w[q] = 1u;
-          if (q < contrib)
-            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w[q]) : "l"(r.zero + (at + q * qs)) : "memory");
+          w0[q] = 1u;
+          w1[q] = 1u;
+          if (q < contrib && v0)
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w0[q]) : "l"(r.zero + (at0 + q * qs)) : "memory");
+          if (q < contrib && v1)
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w1[q]) : "l"(r.zero + (at1 + q * qs)) : "memory");
         }
         for (unsigned it = 0;; ++it) {
           bool all = true;
 #pragma unroll
-          for (int q = 1; q < 16; ++q) all = all && w[q] != 0u;
+          for (int q = 1; q < 16; ++q) all = all && w0[q] != 0u && w1[q] != 0u;
           if (all) break;
           if (it >= kSpinLimit || *aborted) {
             ok = false;
@@ -647,22 +730,33 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
           }
           __nanosleep(32);
 #pragma unroll
-          for (int q = 1; q < 16; ++q)
-            if (q < contrib && w[q] == 0u)
-              asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w[q]) : "l"(r.zero + (at + q * qs)) : "memory");
+          for (int q = 1; q < 16; ++q) {
+            if (q < contrib && w0[q] == 0u)
+              asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w0[q]) : "l"(r.zero + (at0 + q * qs)) : "memory");
+            if (q < contrib && w1[q] == 0u)
+              asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(w1[q]) : "l"(r.zero + (at1 + q * qs)) : "memory");
+          }
         }
         if (!ok) continue;
-        float s = __fadd_rn(0.0f, vown[nt][i]);
+        float s0 = __fadd_rn(0.0f, vown[nt][b]), s1 = __fadd_rn(0.0f, vown[nt][b + 2]);
 #pragma unroll
         for (int q = 1; q < 16; ++q)
           if (q < contrib) {
-            s = __fadd_rn(s, __uint_as_float(~w[q]));
-            asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(r.zero + (at + q * qs)), "r"(0u) : "memory");
+            s0 = __fadd_rn(s0, __uint_as_float(~w0[q]));
+            s1 = __fadd_rn(s1, __uint_as_float(~w1[q]));
+            if (v0)
+              asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(r.zero + (at0 + q * qs)), "r"(0u) : "memory");
+            if (v1)
+              asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(r.zero + (at1 + q * qs)), "r"(0u) : "memory");
           }
-        if (EPI == kEpiGlu)
-          fin[nt][i] = out_value<EPI>(p, row, token, s, gd);
-        else
-          p.y[int64_t(token) * p.n + row] = f32_to_bf16_rn(out_value<EPI>(p, row, token, s, gd));
+        const int64_t row0 = rb * Geo<RG>::kRB + rl0, row1 = row0 + 8;
+        if (EPI == kEpiGlu) {
+          fin[nt][b] = out_value<EPI>(p, row0, token, s0, gd);
+          fin[nt][b + 2] = out_value<EPI>(p, row1, token, s1, gd);
+        } else {
+          if (v0) p.y[int64_t(token) * p.n + row0] = f32_to_bf16_rn(out_value<EPI>(p, row0, token, s0, gd));
+          if (v1) p.y[int64_t(token) * p.n + row1] = f32_to_bf16_rn(out_value<EPI>(p, row1, token, s1, gd));
+        }
       }
     have = ok;
     if (!ok && !*aborted) {
@@ -670,7 +764,7 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
       raise_status(r.status, kDevTimeout);
     }
   } else if (reducer) {
-    uint32_t *flag = r.tickets + rb * kRG + rg;
+    uint32_t *flag = r.tickets + rb * Geo<RG>::kRG + rg;
     bool ok = true;
     if (lane == 0) {
       const unsigned want = unsigned(contrib - 1);
@@ -692,16 +786,16 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
     __syncwarp();  // every lane's loads below follow lane 0's acquire
     if (ok) {
-      const int64_t qs = int64_t(kRB) * 16;
+      const int64_t qs = int64_t(Geo<RG>::kRB) * 16;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int token = nt * 8 + 2 * c + (i & 1);
           const int row_local = rg * 16 + sg + 8 * (i >> 1);
-          const int64_t row = rb * kRB + row_local;
+          const int64_t row = rb * Geo<RG>::kRB + row_local;
           if (token >= m || row >= p.n) continue;
-          const float *src = r.partial + (rb * p.max_contrib * kRB + row_local) * 16 + token;
+          const float *src = r.partial + (rb * p.max_contrib * Geo<RG>::kRB + row_local) * 16 + token;
           float s = __fadd_rn(0.0f, vown[nt][i]);
           if (contrib <= 16) {
             float v[16];
@@ -711,7 +805,15 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
             for (int q = 1; q < 16; ++q)
               if (q < contrib) s = __fadd_rn(s, v[q]);
           } else {
-            for (int q = 1; q < contrib; ++q) s = __fadd_rn(s, __ldcg(src + q * qs));
+            // sixteen loads in flight at a time, added in contributor order
+            for (int q0 = 1; q0 < contrib; q0 += 16) {
+              float v[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v[j] = q0 + j < contrib ? __ldcg(src + (q0 + j) * qs) : 0.0f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                if (q0 + j < contrib) s = __fadd_rn(s, v[j]);
+            }
           }
           if (EPI == kEpiGlu)
             fin[nt][i] = out_value<EPI>(p, row, token, s, gd);
@@ -726,7 +828,7 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
   if (EPI == kEpiGlu && have) {
     // rows sg (gate) and sg + 8 (up) of the row group pair up: output column
     // j = rb * 64 + rg * 8 + sg of h [m, n / 2]
-    const int64_t j = rb * (kRB / 2) + rg * 8 + sg;
+    const int64_t j = rb * (Geo<RG>::kRB / 2) + rg * 8 + sg;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -740,15 +842,16 @@ __device__ __forceinline__ void finish_rows(const Proj &p, const Run &r, int64_t
 }
 
 // Consumers: the whole of this CTA's share of projection p -- activation
-// staging, the unit loop, and the split-K epilogue.  Called by the kW
+// staging, the unit loop, and the split-K epilogue.  Called by the RG
 // consumer warps only.
-// pdl: wait for the previous kernel on the stream (programmatic dependent
-// launch) once everything that does not read its results is worked out.
+// dep: what to wait for before reading x (the previous kernel on the
+// stream, or the previous projection's completion counter), done once
+// everything that does not read its results is worked out.
 // BD: one token (NT == 1, m == 1) in the block-diagonal form of unit_mma_bd.
-template <int NT, int EPI = kEpiPlain, bool BD = false>
+template <int NT, int EPI = kEpiPlain, bool BD = false, int RG = 8>
 __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *base, Ctrl &ct,
                                         uint16_t *xs, RingPos &pos, volatile int *aborted,
-                                        bool pdl = false) {
+                                        const Dep &dep = Dep()) {
   static_assert(!BD || NT == 1, "the block-diagonal form serves one token");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
@@ -771,7 +874,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
   for (int t = 0; t < 2; ++t) {
     off_lo[t] = (rg * 16 + sg) * kUnitCols + (((t * 4 + c) ^ sg) << 4);
     off_hi[t] = (rg * 16 + sg + 8) * kUnitCols + (((t * 4 + c) ^ sg) << 4);
-    off_sc[t] = kPackedStage + rg * (kKT * 128) + t * 128 + (4 * sg + c) * 4;
+    off_sc[t] = Geo<RG>::kPackedStage + rg * (kKT * 128) + t * 128 + (4 * sg + c) * 4;
   }
 
   // -- which k-units this CTA touches: all of them when its range covers a
@@ -793,13 +896,13 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
   //    columns (a function of the token's own data and the partition only,
   //    never of m).
   const int nv_all = slots * (kUnitK / 8);  // 16-byte vectors per token
-  const int per = (nv_all + kW * 32 - 1) / (kW * 32);
+  const int per = (nv_all + Geo<RG>::kW * 32 - 1) / (Geo<RG>::kW * 32);
   constexpr int kV = 4;
   const bool in_regs = NT == 1 && full && m <= 2 && m * per <= 4;
   int kk_of[kV];  // column of each register-staged vector (-1: none)
 #pragma unroll
   for (int j = 0; j < kV; ++j) {
-    const int tok = j / per, v = threadIdx.x + (j - tok * per) * kW * 32;
+    const int tok = j / per, v = threadIdx.x + (j - tok * per) * Geo<RG>::kW * 32;
     kk_of[j] = -1;
     if (in_regs && tok < m && v < nv_all) {
       const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
@@ -808,10 +911,13 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
       if (kk < p.k) kk_of[j] = kk;
     }
   }
-  if (pdl) pdl_wait();
+  if (dep.kind == kDepPdl)
+    pdl_wait();
+  else if (dep.kind == kDepCounter)
+    wait_counter<RG>(dep, aborted, r.status);
   if (in_regs) {
     // Few vectors per thread: they stay in registers from the load to the
-    // f16 store.  Each warp leaves its maximum per token in xmax[tok * kW +
+    // f16 store.  Each warp leaves its maximum per token in xmax[tok * RG +
     // warp]; after one barrier every thread derives the shift itself.
     uint4 q[kV];
     uint32_t mx0 = 0, mx1 = 0;
@@ -836,32 +942,32 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
     }
     if (lane == 0) {
       ct.xmax[warp] = mx0;
-      if (m == 2) ct.xmax[kW + warp] = mx1;
+      if (m == 2) ct.xmax[Geo<RG>::kW + warp] = mx1;
     }
-    consumer_sync();
+    consumer_sync<RG>();
     int sh[2] = {0, 0};
 #pragma unroll
     for (int tok = 0; tok < 2; ++tok) {
       if (tok >= m) break;
       uint32_t b = 0;
 #pragma unroll
-      for (int w2 = 0; w2 < kW; ++w2) b = max(b, ct.xmax[tok * kW + w2]);
+      for (int w2 = 0; w2 < Geo<RG>::kW; ++w2) b = max(b, ct.xmax[tok * RG + w2]);
       if (b != 0 && b < 0x7F80u) sh[tok] = 14 - ilogbf(__uint_as_float(b << 16));
       if (threadIdx.x == tok) ct.shift[tok] = sh[tok];
     }
 #pragma unroll
     for (int j = 0; j < kV; ++j) {
-      const int tok = j / per, v = threadIdx.x + (j - tok * per) * kW * 32;
+      const int tok = j / per, v = threadIdx.x + (j - tok * per) * Geo<RG>::kW * 32;
       if (tok < m && v < nv_all)
         *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) =
             scale_to_f16(q[j], tok == 0 ? sh[0] : sh[1]);
     }
-    consumer_sync();
+    consumer_sync<RG>();
   } else {
     // In full mode the raw bf16 values land in shared memory on the same
     // pass and are converted in place afterwards.
     if (threadIdx.x < 16) ct.xmax[threadIdx.x] = 0;
-    consumer_sync();
+    consumer_sync<RG>();
     {
       const int nv = nv_all;
       for (int tok = 0; tok < m; ++tok) {
@@ -871,11 +977,11 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
         // shared-memory store (the stores go through generic pointers, which
         // would otherwise keep each load waiting for the previous store)
         constexpr int kV = 4;
-        for (int v0 = threadIdx.x; v0 < nv; v0 += kV * kW * 32) {
+        for (int v0 = threadIdx.x; v0 < nv; v0 += kV * Geo<RG>::kW * 32) {
           uint4 q[kV];
 #pragma unroll
           for (int i = 0; i < kV; ++i) {
-            const int v = v0 + i * kW * 32;
+            const int v = v0 + i * Geo<RG>::kW * 32;
             const int s = v / (kUnitK / 8), within = (v % (kUnitK / 8)) * 8;
             const int uk = all_units ? s : (uk_begin + s) % units;
             const int kk = uk * kUnitK + within;
@@ -884,7 +990,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
           }
 #pragma unroll
           for (int i = 0; i < kV; ++i) {
-            const int v = v0 + i * kW * 32;
+            const int v = v0 + i * Geo<RG>::kW * 32;
             if (v >= nv) break;
             mx = absmax8(mx, q[i]);
             if (full) *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) = q[i];
@@ -896,24 +1002,24 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
         if (lane == 0 && mx != 0) atomicMax(&ct.xmax[tok], mx);
       }
     }
-    consumer_sync();
+    consumer_sync<RG>();
     if (threadIdx.x < m) {
       const uint32_t b = ct.xmax[threadIdx.x];
       int sh = 0;
       if (b != 0 && b < 0x7F80u) sh = 14 - ilogbf(__uint_as_float(b << 16));
       ct.shift[threadIdx.x] = sh;
     }
-    consumer_sync();
+    consumer_sync<RG>();
     if (full) {
       const int nv = nv_all;
       for (int tok = 0; tok < m; ++tok) {
         const int sh = ct.shift[tok];
-        for (int v = threadIdx.x; v < nv; v += kW * 32) {
+        for (int v = threadIdx.x; v < nv; v += Geo<RG>::kW * 32) {
           uint4 *q = reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8));
           *q = scale_to_f16(*q, sh);  // written by this same thread above
         }
       }
-      consumer_sync();
+      consumer_sync<RG>();
     }
   }
   const float gd = __ldg(p.g_dec);
@@ -952,9 +1058,9 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
     for (int cu0 = uk0; cu0 < uk1; cu0 += step_units) {
       const int cu1 = min(uk1, cu0 + step_units);
       if (!full) {
-        consumer_sync();  // earlier readers of the staging buffer are done
+        consumer_sync<RG>();  // earlier readers of the staging buffer are done
         const int nv = (cu1 - cu0) * (kUnitK / 8);
-        for (int idx = threadIdx.x; idx < m * nv; idx += kW * 32) {
+        for (int idx = threadIdx.x; idx < m * nv; idx += Geo<RG>::kW * 32) {
           const int tok = idx / nv, v = idx - tok * nv;
           const int kk = cu0 * kUnitK + v * 8;
           uint4 q = make_uint4(0, 0, 0, 0);
@@ -962,7 +1068,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
           *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) =
               scale_to_f16(q, ct.shift[tok]);
         }
-        consumer_sync();
+        consumer_sync<RG>();
       }
 
       // staged slot of unit cu0 (slots follow units, wrapping at `units`)
@@ -975,7 +1081,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
         uint32_t sw[2] = {0, 0};
         const bool ok = !*aborted && mbar_wait(&ct.full[st], pos.phase, aborted);
         if (ok) {
-          const uint8_t *stage = base + st * kStageBytes;
+          const uint8_t *stage = base + st * Geo<RG>::kStageBytes;
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             wlo[t] = *reinterpret_cast<const uint4 *>(stage + off_lo[t]);
@@ -1046,7 +1152,7 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
     }
     // (two token blocks: the shares are worked out again, which keeps
     // their registers free through the unit loop)
-    finish_rows<NT, EPI>(p, r, rb, complete, v, gd, rg, sg, lane, aborted,
+    finish_rows<NT, EPI, RG>(p, r, rb, complete, v, gd, rg, sg, lane, aborted,
                          NT > 1 ? 0 : complete ? 1 : (rb == rb0 ? contrib0 : contrib1),
                          complete ? 0 : (rb == rb0 ? jj0 : jj1));
     u += uk1 - uk0;
@@ -1061,18 +1167,20 @@ struct SmemView {
   Ctrl *ct;
   uint16_t *xs;
 };
+template <int RG = 8>
 __device__ __forceinline__ SmemView carve(uint8_t *raw, int stages) {
   SmemView v;
   v.base = raw + ((1024u - (smem_u32(raw) & 1023u)) & 1023u);
-  v.ct = reinterpret_cast<Ctrl *>(v.base + stages * kStageBytes);
-  v.xs = reinterpret_cast<uint16_t *>(v.base + stages * kStageBytes + kCtrlBytes);
+  v.ct = reinterpret_cast<Ctrl *>(v.base + stages * Geo<RG>::kStageBytes);
+  v.xs = reinterpret_cast<uint16_t *>(v.base + stages * Geo<RG>::kStageBytes + kCtrlBytes);
   return v;
 }
 
+template <int RG = 8>
 __device__ __forceinline__ void init_ring(Ctrl &ct, int S) {
   for (int s = 0; s < S; ++s) {
     mbar_init(&ct.full[s], 1);
-    mbar_init(&ct.empty[s], kW);
+    mbar_init(&ct.empty[s], Geo<RG>::kW);
   }
   ct.aborted = 0;
   ct.zero = make_uint4(0, 0, 0, 0);
@@ -1082,9 +1190,9 @@ __device__ __forceinline__ void init_ring(Ctrl &ct, int S) {
 #endif  // __CUDACC__
 
 // Host-side helpers shared by the launchers.
-size_t smem_bytes(int stages, int x_cap_halves);
-int stages_for(int x_cap_halves);
-bool encode_maps(const aq_nvfp4_weight &w, CUtensorMap *tm_w, CUtensorMap *tm_s);
+size_t smem_bytes(int stages, int x_cap_halves, int rg);
+int stages_for(int x_cap_halves, int rg);
+bool encode_maps(const aq_nvfp4_weight &w, CUtensorMap *tm_w, CUtensorMap *tm_s, int rg);
 bool encode_bf16_map(const uint16_t *w, int n, int k, CUtensorMap *tm);
 
 }  // namespace core

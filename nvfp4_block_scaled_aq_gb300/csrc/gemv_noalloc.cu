@@ -33,7 +33,9 @@ bool g_ready[kMaxDevices];
 
 // First call on a device (that device current): resolve the array's device
 // address and zero it once.  Synchronous: the first call on each device
-// must not be made while a stream is being captured.
+// must not be made while a stream is being captured.  The address is kept
+// for the life of the process; a cudaDeviceReset reloads the module at a
+// new address, so the call must not be used across a device reset.
 aq_status scratch_for(const DeviceInfo &dev, uint8_t **out) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (dev.ordinal < 0 || dev.ordinal >= kMaxDevices)
@@ -64,11 +66,13 @@ aq_status aq_gemv_nvfp4_noalloc(const aq_nvfp4_weight *w, const uint16_t *x, int
   aq_status s = gemv_args(w, x, m, y, path, what);
   if (s != AQ_OK) return s;
   if (path == AQ_PATH_GEMV_TCGEN05 || path == AQ_PATH_MMA || m > AQ_MAX_M)
-    return set_error(AQ_ERR_UNSUPPORTED, "%s: runs the register-decode kernel only (m <= %d)",
+    return set_error(AQ_ERR_UNSUPPORTED,
+                     "%s: runs the register-decode kernel only (m <= %d, no MMA or tcgen05 path)",
                      what, AQ_MAX_M);
   const DeviceInfo *dev = device_info();
   if (!dev) return AQ_ERR_UNSUPPORTED;
-  const size_t need = gemv_workspace_bytes(w->n, w->k, *dev);
+  // only the register-decode kernel runs here, so only its scratch counts
+  const size_t need = gemv_regdecode_workspace_bytes(w->n, w->k, *dev);
   if (need > AQ_GEMV_NOALLOC_MAX_SCRATCH)
     return set_error(AQ_ERR_WORKSPACE,
                      "%s: a [%d, %d] weight needs %zu bytes of scratch on this device, more than "
@@ -82,12 +86,13 @@ aq_status aq_gemv_nvfp4_noalloc(const aq_nvfp4_weight *w, const uint16_t *x, int
   // on a bounded wait may not, so the part of both that this weight uses is
   // cleared on the stream before every launch; the plain partials after
   // them are always written before they are read.
-  const GemvPlan plan = plan_gemv(w->n, w->k, *dev);
-  const size_t tickets = size_t(plan.row_blocks) * kTicketsPerRowBlock * sizeof(uint32_t);
+  const GemvPlan plan = plan_gemv(w->n, w->k, *dev, kGemvRG);
+  const size_t tickets = size_t(plan.row_blocks) * kGemvRG * sizeof(uint32_t);
   cudaError_t e = cudaMemsetAsync(scratch, 0, tickets, st);
-  if (e == cudaSuccess && core::direct_partials_fit(plan.row_blocks, plan.max_contrib, m))
+  if (e == cudaSuccess && core::direct_partials_fit<kGemvRG>(plan.row_blocks, plan.max_contrib, m))
     e = cudaMemsetAsync(scratch + core::kTicketBytes, 0,
-                        size_t(plan.row_blocks) * (plan.max_contrib - 1) * m * core::kRB * 4, st);
+                        size_t(plan.row_blocks) * (plan.max_contrib - 1) * m * (16 * kGemvRG) * 4,
+                        st);
   if (e != cudaSuccess) return cuda_error(e, what);
   e = launch_gemv_uncached(*w, x, m, y, scratch, *dev, st);
   return e == cudaSuccess ? AQ_OK : cuda_error(e, what);

@@ -388,7 +388,7 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 // mma_n(m) >= 16 token slots, then the quantised activations (packed,
 // scales, g_dec), each 256-byte aligned.
 MmaWorkspace mma_workspace(int n, int k, int m, const DeviceInfo &dev) {
-  const GemvPlan p = plan_gemv(n, k, dev);
+  const GemvPlan p = plan_gemv(n, k, dev, 8);
   MmaWorkspace w;
   w.slots = mma_n(m) < 16 ? 16 : mma_n(m);
   w.scale_pitch = (k / 16 + 15) / 16 * 16;
@@ -418,10 +418,10 @@ cudaError_t launch_mma(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint1
   cudaError_t e = launch_act_quant(x, m, w.k, xq, xs, lay.scale_pitch, xg, dev, st);
   if (e != cudaSuccess) return e;
 
-  const GemvPlan plan = plan_gemv(w.n, w.k, dev);
+  const GemvPlan plan = plan_gemv(w.n, w.k, dev, 8);
   const int N = mma_n(m);
   CUtensorMap tm_w, tm_s, tm_x, tm_xs;
-  if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
+  if (!encode_maps(w, &tm_w, &tm_s, 8)) return cudaErrorInvalidValue;
   if (!encode_act_maps(xq, xs, m, w.k, lay.scale_pitch, N, &tm_x, &tm_xs))
     return cudaErrorInvalidValue;
   Run r{};

@@ -591,7 +591,7 @@ cudaError_t launch_gemv_tc(const aq_nvfp4_weight &w, const uint16_t *x, int m, u
                            void *ws, bool pdl, const DeviceInfo &dev, cudaStream_t st) {
   const GemvPlan plan = plan_gemv_tc(w.n, w.k, dev);
   CUtensorMap tm_w, tm_s;
-  if (!encode_maps(w, &tm_w, &tm_s)) return cudaErrorInvalidValue;
+  if (!encode_maps(w, &tm_w, &tm_s, 8)) return cudaErrorInvalidValue;
   const int64_t longest = ceil_div(plan.total, plan.grid);
   const int slots = x_slots(longest, int(plan.units));
   Run r{};

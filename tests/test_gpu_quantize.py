@@ -181,3 +181,24 @@ def test_fused_reconstruct_quantize_bit_exact(n, k, r, passthrough):
     if passthrough:
         assert np.array_equal(W_eff, bits(th.W0))
     assert_quantized_equal(w, W_eff)
+
+
+def test_rank4_v_not_8_byte_aligned_bit_exact():
+    """A rank-4 V that is only 2-byte aligned (a view one bf16 into a larger
+    buffer) takes the generic rank path of both the reconstruction and the
+    fused reconstruct-and-quantise; both stay bit-exact with the oracle."""
+    n, k, r = 48, 160, 4
+    th = inputs.theta(n, k, r, seed=77, device=DEV)
+    big = torch.empty(k * r + 8, dtype=torch.bfloat16, device=DEV)
+    V = big[1:1 + k * r].view(k, r)
+    V.copy_(th.V)
+    assert V.data_ptr() % 8 == 2
+    ref = oracle.reconstruct(bits(th.W0), th.s.cpu().numpy(), bits(th.U), bits(th.V))
+    W_eff = torch.empty((n, k), dtype=torch.bfloat16, device=DEV)
+    aq.reconstruct(th.W0, th.s, th.U, V, W_eff)
+    assert np.array_equal(bits(W_eff), ref)
+    w = aq.Nvfp4Weight.empty(n, k, device=DEV)
+    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    aq.reconstruct_quantize(th.W0, th.s, th.U, V, w, ws)
+    assert_quantized_equal(w, ref)
+    assert aq.poll_device_status() == aq.OK

@@ -94,10 +94,11 @@ def test_full_1b_step_against_oracle():
 
 # ------------------------------------------------------------ persistent step
 
-@pytest.mark.parametrize("m", [1, 3])
+@pytest.mark.parametrize("m", [1, 3, 12])
 def test_persistent_step_matches_oracle_and_separate_calls(m):
     """One cooperative launch for the whole stack: every projection within
-    tolerance of the oracle, and of the per-projection launches."""
+    tolerance of the oracle, and equal bit for bit to the per-projection
+    launch on the register-decode kernel (same partition, same form)."""
     Ws, ws, xs, ys = build_stack(3, inputs.LAYER_1B, m, seed=11)
     plan = aq.StepPlan(ws, xs, ys)
     wsp = plan.workspace()
@@ -108,7 +109,17 @@ def test_persistent_step_matches_oracle_and_separate_calls(m):
         packed, scales, ge, gd = oracle.quantize(bits(W))
         y_ref = oracle.gemv(packed, scales, gd, bits(x))
         assert_gemv_close(y, y_ref, "projection %d" % i)
-        assert_gemv_close(gemv_gpu(w, x), y_ref, "separate %d" % i)
+        assert torch.equal(y, gemv_gpu(w, x, path=aq.PATH_GEMV_REGDECODE)), "projection %d" % i
+    # the counters are back at zero: a second run on the same workspace
+    # gives the same bits
+    first = [y.clone() for y in ys]
+    for y in ys:
+        y.zero_()
+    aq.step_run(plan, wsp)
+    torch.cuda.synchronize()
+    assert aq.poll_device_status() == aq.OK
+    for a, b in zip(ys, first):
+        assert torch.equal(a, b)
 
 
 def test_persistent_step_repeats_bit_exact_and_is_m_invariant():
@@ -203,3 +214,60 @@ def test_step_rejects_two_kernel_flags():
     with pytest.raises(aq.AqError) as e:
         aq.decode_step(aq.StepArgs(ws, xs, ys), wsp, flags=aq.STEP_REGDECODE | aq.STEP_MMA)
     assert e.value.status == aq.ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------ full size, bench path
+
+def _sampled_31b_check(Ws_bits, ws, xs, ys, layers, what):
+    rng = np.random.default_rng(31)
+    for i in range(layers * 4):
+        n, k = inputs.LAYER_31B[i % 4]
+        Wb = Ws_bits[i]
+        ge, gd = oracle.global_scales(oracle.amax(Wb))
+        rows = np.sort(rng.choice(n, 256, replace=False))
+        packed_r, scales_r = oracle.quantize_rows(Wb[rows], ge)
+        y_ref = oracle.gemv(packed_r, scales_r, gd, bits(xs[i]))
+        assert_gemv_close(ys[i][:, rows], y_ref, "%s, projection %d" % (what, i))
+
+
+def test_31b_step_pdl_graph_sampled_parity():
+    """Two layers of the ~31B-shaped stack at full size through the timed
+    path of the benchmark: aq_decode_step_weights with programmatic
+    dependent launch and the next-projection L2 prefetch, captured in a CUDA
+    graph and replayed; 256 seeded rows of every projection against the
+    oracle."""
+    layers, m = 2, 1
+    Ws_bits, ws, xs, ys = [], [], [], []
+    for layer in range(layers):
+        for p, (n, k) in enumerate(inputs.LAYER_31B):
+            W = inputs.weight(n, k, seed=inputs.seed_of(0, layer, p), device=DEV)
+            ws.append(quantize_gpu(W))
+            Ws_bits.append(bits(W))
+            del W
+            xs.append(inputs.tokens(m, k, seed=inputs.seed_of(1, layer, p), device=DEV))
+            ys.append(torch.full((m, n), float("nan"), dtype=torch.bfloat16, device=DEV))
+    wsp = step_workspace(inputs.LAYER_31B, m)
+    args = aq.StepArgs(ws, xs, ys)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        aq.decode_step(args, wsp, flags=aq.STEP_PDL | aq.STEP_REGDECODE, stream=side)
+        side.synchronize()
+        for y in ys:
+            y.fill_(float("nan"))
+        with torch.cuda.graph(graph, stream=side):
+            aq.decode_step(args, wsp, flags=aq.STEP_PDL | aq.STEP_REGDECODE, stream=side)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert aq.poll_device_status() == aq.OK
+    _sampled_31b_check(Ws_bits, ws, xs, ys, layers, "PDL graph")
+    # the persistent step on the same stack: the same bits
+    chain = [y.clone() for y in ys]
+    plan = aq.StepPlan(ws, xs, ys)
+    aq.step_run(plan, plan.workspace())
+    torch.cuda.synchronize()
+    assert aq.poll_device_status() == aq.OK
+    for i, (a, b) in enumerate(zip(ys, chain)):
+        assert torch.equal(a, b), "persistent step differs from the chain at projection %d" % i

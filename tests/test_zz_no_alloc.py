@@ -1,7 +1,8 @@
 """aq_gemv_nvfp4_noalloc: the GEMV for callers that cannot allocate device
 memory.  Its split-K scratch is a fixed array inside the library, so the
-call takes no workspace; its output must agree with aq_gemv_nvfp4 (which
-uses a caller workspace) within the GEMV tolerance, call after call.
+call takes no workspace; its output must equal aq_gemv_nvfp4 on the same
+(register-decode) kernel with a caller workspace bit for bit, call after
+call, and so also stay within the GEMV tolerance of that output.
 
 The file name makes pytest collect it last, so it runs both after every
 other test in the session and, run on its own, as the first library call
@@ -49,7 +50,27 @@ def test_noalloc_matches_workspace_gemv_on_consecutive_calls():
         torch.cuda.synchronize()
         assert aq.poll_device_status() == aq.OK
         for i, (y, ref) in enumerate(zip(outs, refs)):
+            # the header promises the workspace call's bits; the tolerance
+            # check is a second, looser statement of the same
+            assert torch.equal(y, ref), "round %d case %d: outputs differ" % (rep, i)
             assert_gemv_close(y, as_ref(ref), "round %d case %d" % (rep, i))
+
+
+def test_noalloc_rejects_paths_it_does_not_run():
+    # m = 17 on AQ_PATH_AUTO would take the MMA path in aq_gemv_nvfp4, and
+    # AQ_PATH_MMA always does; this entry point runs the register-decode
+    # kernel only, so both are refused on the host before any launch
+    n, k = 256, 512
+    w = quantize_gpu(inputs.weight(n, k, seed=5, device=DEV))
+    for m, path in ((17, aq.PATH_AUTO), (4, aq.PATH_MMA), (2, aq.PATH_GEMV_TCGEN05)):
+        x = inputs.tokens(m, k, seed=6, device=DEV)
+        y = torch.zeros((m, n), dtype=torch.bfloat16, device=DEV)
+        with pytest.raises(aq.AqError) as exc:
+            aq.gemv_noalloc(w, x, y, path=path)
+        assert exc.value.status == aq.ERR_UNSUPPORTED, (m, path)
+        assert "register-decode" in str(exc.value)
+        assert not y.any()
+    assert aq.poll_device_status() == aq.OK
 
 
 def test_noalloc_rejects_a_weight_beyond_the_scratch():
