@@ -66,8 +66,8 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
   return r;
 }
 
-// Two non-negative fp32 -> one byte of two E2M1 codes (nearest even,
-// saturate to 6): `hi` goes to the high nibble.
+// Two fp32 -> one byte of two E2M1 codes (nearest even, saturate to +-6,
+// sign kept): `hi` goes to the high nibble.
 __device__ __forceinline__ uint32_t f32x2_to_e2m1x2(float hi, float lo) {
   uint32_t r;
   asm("{ .reg .b8 t;\n"

@@ -30,7 +30,7 @@ constexpr int kMaxStages = 6;
 constexpr int kMinStages = 2;
 constexpr int kCtasPerSm = 2;
 constexpr int kSmemBudget = 113 * 1024;         // per CTA, so two fit on an SM
-constexpr int kXChunkBudget = 16;               // m * units staged at once (chunked mode)
+constexpr int kXChunkBudget = 64;               // m * units staged at once (chunked mode)
 constexpr int kTileHalves = 128;                // f16 per staged 128-column tile
 constexpr unsigned kSpinLimit = 1u << 22;
 // Layout of every GEMV workspace:
@@ -1059,14 +1059,31 @@ __device__ __forceinline__ void consume(const Proj &p, const Run &r, uint8_t *ba
       const int cu1 = min(uk1, cu0 + step_units);
       if (!full) {
         consumer_sync<RG>();  // earlier readers of the staging buffer are done
+        // four vectors per thread per round, all loaded before any is
+        // converted and stored (a store through a generic pointer would
+        // otherwise hold the next load back until it completes)
         const int nv = (cu1 - cu0) * (kUnitK / 8);
-        for (int idx = threadIdx.x; idx < m * nv; idx += Geo<RG>::kW * 32) {
-          const int tok = idx / nv, v = idx - tok * nv;
-          const int kk = cu0 * kUnitK + v * 8;
-          uint4 q = make_uint4(0, 0, 0, 0);
-          if (kk < p.k) q = __ldg(reinterpret_cast<const uint4 *>(p.x + int64_t(tok) * p.k + kk));
-          *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) =
-              scale_to_f16(q, ct.shift[tok]);
+        constexpr int kCV = 4;
+        constexpr int kStep = Geo<RG>::kW * 32;
+        for (int base = threadIdx.x; base < m * nv; base += kCV * kStep) {
+          uint4 q[kCV];
+#pragma unroll
+          for (int i = 0; i < kCV; ++i) {
+            const int idx = base + i * kStep;
+            const int tok = idx / nv, v = idx - tok * nv;
+            const int kk = cu0 * kUnitK + v * 8;
+            q[i] = make_uint4(0, 0, 0, 0);
+            if (idx < m * nv && kk < p.k)
+              q[i] = __ldg(reinterpret_cast<const uint4 *>(p.x + int64_t(tok) * p.k + kk));
+          }
+#pragma unroll
+          for (int i = 0; i < kCV; ++i) {
+            const int idx = base + i * kStep;
+            if (idx >= m * nv) break;
+            const int tok = idx / nv, v = idx - tok * nv;
+            *reinterpret_cast<uint4 *>(xs + tok * stride + x_off(v * 8)) =
+                scale_to_f16(q[i], ct.shift[tok]);
+          }
         }
         consumer_sync<RG>();
       }

@@ -188,10 +188,9 @@ __device__ __forceinline__ uint32_t quantize_block(const float *w, float g_enc,
     for (int i = 0; i < 8; ++i) {
       const float v0 = __fmul_rn(w[2 * i], rcp);
       const float v1 = __fmul_rn(w[2 * i + 1], rcp);
-      uint32_t byte = f32x2_to_e2m1x2(fabsf(v1), fabsf(v0));
-      byte |= (__float_as_uint(v0) >> 31) << 3;
-      byte |= (__float_as_uint(v1) >> 31) << 7;
-      bytes[i] = byte;
+      // the conversion keeps the sign, a negative value that rounds to zero
+      // included (nibble 0x8); the sweep over every bf16 value checks it
+      bytes[i] = f32x2_to_e2m1x2(v1, v0);
     }
     lo = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
     hi = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
@@ -270,6 +269,202 @@ __global__ void __launch_bounds__(kThreads)
       sword |= (sf0 | (sf1 << 8)) << (16 * h);
     }
     reinterpret_cast<uint32_t *>(scales + tile * 128)[lane] = sword;
+  }
+}
+
+// ---------------------------------------------------------- rank 4, V reused
+// The fused form for the configured rank (4) with V 16-byte aligned.  Each
+// warp keeps one 128-column tile column for its whole life and walks down
+// its row tiles (warps w and w + P * tiles_k share a tile column; P row
+// tiles are in flight per column), so the V rows it reads stay in L1; per
+// 16-column block lane (g, c) loads the block's V rows once (128 bytes,
+// eight 16-byte loads) and rebuilds rows g and g + 8 from them.  The
+// arithmetic is recon_elem<4>'s, in the same order.
+
+// One element of the rank-4 rebuild (fp32, before the bf16 rounding) from V
+// values already in registers: recon_elem<4>'s value.  The zero-delta case
+// (s * w0 alone) is one fma with -0 as the addend: fma(s, w0, -0) is the
+// product rounded once, -0 when the product is -0 and +0 when it is +0,
+// exactly as the rounded product itself.
+__device__ __forceinline__ float recon4(float w0, float s, const float (&u)[4], uint32_t v01,
+                                        uint32_t v23) {
+  float delta = 0.0f;
+  delta = __fmaf_rn(u[0], bf16_lo(v01), delta);
+  delta = __fmaf_rn(u[1], bf16_hi(v01), delta);
+  delta = __fmaf_rn(u[2], bf16_lo(v23), delta);
+  delta = __fmaf_rn(u[3], bf16_hi(v23), delta);
+  return __fmaf_rn(s, w0, delta == 0.0f ? -0.0f : delta);
+}
+
+// Two fp32 -> bf16x2 (nearest even), `hi` in the upper half.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float hi, float lo) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// V rows of the 16 columns starting at col: column j's four entries in
+// vr[2j] (entries 0, 1) and vr[2j + 1] (entries 2, 3).
+__device__ __forceinline__ void load_v16(const uint16_t *__restrict__ V, int64_t col,
+                                         uint32_t (&vr)[32]) {
+  const uint4 *src = reinterpret_cast<const uint4 *>(V + col * 4);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 v = __ldg(src + i);
+    vr[4 * i] = v.x;
+    vr[4 * i + 1] = v.y;
+    vr[4 * i + 2] = v.z;
+    vr[4 * i + 3] = v.w;
+  }
+}
+
+// The 16 rebuilt values (bf16-rounded, as fp32) of row `row`, columns
+// col .. col + 15.
+__device__ __forceinline__ void rebuild16(const uint16_t *__restrict__ W0, float srow,
+                                          const float (&u)[4], int k, int64_t row, int64_t col,
+                                          const uint32_t (&vr)[32], float (&w)[16]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(W0 + row * k + col) + q);
+    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = 8 * q + 2 * i;
+      const float lo = recon4(bf16_lo(vv[i]), srow, u, vr[2 * j], vr[2 * j + 1]);
+      const float hi = recon4(bf16_hi(vv[i]), srow, u, vr[2 * j + 2], vr[2 * j + 3]);
+      const uint32_t b2 = f32x2_to_bf16x2(hi, lo);
+      w[j] = bf16_lo(b2);
+      w[j + 1] = bf16_hi(b2);
+    }
+  }
+}
+
+// max over the 16 values of |e| (fp32, before the bf16 rounding) as bit
+// patterns with the sign cleared, so a NaN or an infinity sorts above every
+// finite value.  Rounding to nearest is monotonic in magnitude, so the
+// largest |bf16(e)| is bf16 of the largest |e|: the caller rounds once.
+__device__ __forceinline__ uint32_t rebuild16_absmax(const uint16_t *__restrict__ W0, float srow,
+                                                     const float (&u)[4], int k, int64_t row,
+                                                     int64_t col, const uint32_t (&vr)[32],
+                                                     uint32_t m) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(W0 + row * k + col) + q);
+    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int j = 8 * q + 2 * i;
+      const float lo = recon4(bf16_lo(vv[i]), srow, u, vr[2 * j], vr[2 * j + 1]);
+      const float hi = recon4(bf16_hi(vv[i]), srow, u, vr[2 * j + 2], vr[2 * j + 3]);
+      m = max(m, __float_as_uint(lo) & 0x7FFFFFFFu);
+      m = max(m, __float_as_uint(hi) & 0x7FFFFFFFu);
+    }
+  }
+  return m;
+}
+
+__device__ __forceinline__ void row_terms(const float *__restrict__ s,
+                                          const uint16_t *__restrict__ U, int64_t row,
+                                          float &srow, float (&u)[4]) {
+  srow = __ldg(s + row);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) u[t] = __uint_as_float(uint32_t(__ldg(U + row * 4 + t)) << 16);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    amax_r4_kernel(const uint16_t *__restrict__ W0, const float *__restrict__ s,
+                   const uint16_t *__restrict__ U, const uint16_t *__restrict__ V, int n,
+                   int k, int rows_in_flight, uint32_t *amax_bits) {
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
+  const int64_t warp = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  uint32_t m = 0;
+  if (warp < tiles_k * rows_in_flight) {
+    const int64_t tk = warp % tiles_k, tn0 = warp / tiles_k;
+    const int64_t col = tk * kTileCols + 32 * c;
+    if (col < k)
+      for (int64_t tn = tn0; tn < tiles_n; tn += rows_in_flight) {
+        float srow[2], u[2][4];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t row = tn * kTileRows + 8 * h + g;
+          if (row < n) row_terms(s, U, row, srow[h], u[h]);
+        }
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+          uint32_t vr[32];
+          load_v16(V, col + 16 * b, vr);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int64_t row = tn * kTileRows + 8 * h + g;
+            if (row >= n) continue;
+            m = rebuild16_absmax(W0, srow[h], u[h], k, row, col + 16 * b, vr, m);
+          }
+        }
+      }
+  }
+  // bf16 bits of the largest |e|: a NaN stays a NaN pattern and an
+  // infinity the infinity pattern, both at or above 0x7F80
+  uint32_t mb = m >= 0x7F800000u ? (m >> 16) | (m > 0x7F800000u ? 0x40u : 0u)
+                                 : uint32_t(f32_to_bf16_rn(__uint_as_float(m)));
+  mb = block_max_u32(mb);
+  if (threadIdx.x == 0) atomicMax(amax_bits, mb);
+}
+
+__global__ void __launch_bounds__(kThreads)
+    quantize_r4_kernel(const uint16_t *__restrict__ W0, const float *__restrict__ s,
+                       const uint16_t *__restrict__ U, const uint16_t *__restrict__ V, int n,
+                       int k, int rows_in_flight, uint8_t *__restrict__ packed,
+                       uint8_t *__restrict__ scales, float *__restrict__ global_scale,
+                       const uint32_t *__restrict__ amax_bits, unsigned *status) {
+  float g_enc = 1.0f, g_dec = 1.0f;
+  const bool ok = global_scales(*amax_bits, g_enc, g_dec);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *global_scale = ok ? g_dec : __int_as_float(0x7FC00000);
+    if (!ok) raise_status(status, kDevRange);
+  }
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
+  const int64_t warp = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
+  if (warp >= tiles_k * rows_in_flight) return;
+  const int64_t tk = warp % tiles_k, tn0 = warp / tiles_k;
+  const int64_t col = tk * kTileCols + 32 * c;
+  for (int64_t tn = tn0; tn < tiles_n; tn += rows_in_flight) {
+    float srow[2], u[2][4];
+    uint32_t out[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+    uint32_t sword = 0;
+    if (col < k) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t row = tn * kTileRows + 8 * h + g;
+        if (row < n) row_terms(s, U, row, srow[h], u[h]);
+      }
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        uint32_t vr[32];
+        load_v16(V, col + 16 * b, vr);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int64_t row = tn * kTileRows + 8 * h + g;
+          if (row >= n) continue;
+          float w[16];
+          rebuild16(W0, srow[h], u[h], k, row, col + 16 * b, vr, w);
+          uint32_t sf = 0;
+          if (ok) sf = quantize_block(w, g_enc, out[h][2 * b], out[h][2 * b + 1]);
+          sword |= sf << (16 * h + 8 * b);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t row = tn * kTileRows + 8 * h + g;
+        if (row < n)
+          *reinterpret_cast<uint4 *>(packed + row * (k / 2) + col / 2) =
+              make_uint4(out[h][0], out[h][1], out[h][2], out[h][3]);
+      }
+    }
+    reinterpret_cast<uint32_t *>(scales + (tn * tiles_k + tk) * 128)[lane] = sword;
   }
 }
 
@@ -374,6 +569,22 @@ static void quantize_pass(const uint16_t *W, const float *s, const uint16_t *U,
                                                      dev.status);
 }
 
+// Rank 4 with V reused per warp: P row tiles in flight per tile column,
+// about sixteen warps per SM in all (two CTAs of eight, one wave).
+static void quantize_pass_r4(const uint16_t *W, const float *s, const uint16_t *U,
+                             const uint16_t *V, int n, int k, const aq_nvfp4_weight &out,
+                             uint32_t *amax, const DeviceInfo &dev, cudaStream_t st) {
+  const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
+  int64_t P = int64_t(dev.sms) * 16 / tiles_k;
+  if (P < 1) P = 1;
+  if (P > tiles_n) P = tiles_n;
+  const int warps_per_cta = kThreads / 32;
+  const int g = int(ceil_div(tiles_k * P, warps_per_cta));
+  amax_r4_kernel<<<g, kThreads, 0, st>>>(W, s, U, V, n, k, int(P), amax);
+  quantize_r4_kernel<<<g, kThreads, 0, st>>>(W, s, U, V, n, k, int(P), out.packed, out.scales,
+                                             out.global_scale, amax, dev.status);
+}
+
 cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U,
                             const uint16_t *V, int r, bool fused, int n, int k,
                             const aq_nvfp4_weight &out, void *ws, const DeviceInfo &dev,
@@ -383,6 +594,8 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
   if (e != cudaSuccess) return e;
   if (!fused)
     quantize_pass<0, false>(W, s, U, V, 0, n, k, out, amax, dev, st);
+  else if (r == 4 && (reinterpret_cast<uintptr_t>(V) & 15u) == 0)
+    quantize_pass_r4(W, s, U, V, n, k, out, amax, dev, st);
   else if (r == 0)
     quantize_pass<0, true>(W, s, U, V, r, n, k, out, amax, dev, st);
   else if (r == 4 && (reinterpret_cast<uintptr_t>(V) & 7u) == 0)

@@ -183,16 +183,19 @@ def test_fused_reconstruct_quantize_bit_exact(n, k, r, passthrough):
     assert_quantized_equal(w, W_eff)
 
 
-def test_rank4_v_not_8_byte_aligned_bit_exact():
+@pytest.mark.parametrize("offset", [1, 4])
+def test_rank4_v_alignment_paths_bit_exact(offset):
     """A rank-4 V that is only 2-byte aligned (a view one bf16 into a larger
-    buffer) takes the generic rank path of both the reconstruction and the
-    fused reconstruct-and-quantise; both stay bit-exact with the oracle."""
+    buffer) takes the generic rank path of the reconstruction and the fused
+    reconstruct-and-quantise; one that is 8- but not 16-byte aligned (four
+    bf16 in) takes the per-element rank-4 path instead of the one that keeps
+    V rows in registers.  Every path stays bit-exact with the oracle."""
     n, k, r = 48, 160, 4
     th = inputs.theta(n, k, r, seed=77, device=DEV)
     big = torch.empty(k * r + 8, dtype=torch.bfloat16, device=DEV)
-    V = big[1:1 + k * r].view(k, r)
+    V = big[offset:offset + k * r].view(k, r)
     V.copy_(th.V)
-    assert V.data_ptr() % 8 == 2
+    assert V.data_ptr() % 16 == 2 * offset
     ref = oracle.reconstruct(bits(th.W0), th.s.cpu().numpy(), bits(th.U), bits(th.V))
     W_eff = torch.empty((n, k), dtype=torch.bfloat16, device=DEV)
     aq.reconstruct(th.W0, th.s, th.U, V, W_eff)
