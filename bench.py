@@ -46,11 +46,9 @@ NCU_TRAFFIC = {
     # weight of the layer can still sit in L2 from an earlier step), m = 1,
     # one-token kernel form, captured without cache flushing so the L2
     # prefetch of the next projection counts where it is issued: reads
-    # 19,086,336 + 15,315,456 + 142,870,272 + 68,184,064, writes 91,136 +
-    # 77,824 + 408,576 + 165,376 (the committed ncu summary of that capture);
-    # the key is of the sources after comment-only edits to gemv.cu, the
-    # device code unchanged since the capture
-    ("gemma4-31b-shaped decode-step weight stream", 1, "83e96172c032b4ac9ada6f291548c27441508458"): 246199040,
+    # 19,208,704 + 14,810,368 + 144,470,528 + 67,886,080, writes 183,296 +
+    # 83,456 + 466,688 + 254,464 (the committed ncu summary of that capture)
+    ("gemma4-31b-shaped decode-step weight stream", 1, "4b88f539555eb6e9b267da702207c4f762e9f0f0"): 247363584,
 }
 
 
@@ -70,11 +68,14 @@ def parse():
     p.add_argument("--sweep-m", type=str, default="",
                    help="comma-separated subset of the sweep's M values (profiling)")
     p.add_argument("--sweep-proj", choices=("both", "gate_up", "down"), default="both")
-    p.add_argument("--kernel", choices=("regdecode", "tcgen05"), default="regdecode",
+    p.add_argument("--kernel", choices=("regdecode", "tcgen05", "mma"), default="regdecode",
                    help="GEMV kernel of the timed step (regdecode: the library's default "
                         "for m <= 16; the other one is timed among the extras)")
     p.add_argument("--bf16-lm-head", action="store_true",
                    help="time only the bf16 GEMV on the ~31B tied lm_head [262144, 5376], m = 1")
+    p.add_argument("--profile-case", choices=("gemv", "load"), default="",
+                   help="a few calls on one ~31B projection, for profilers (not a timing)")
+    p.add_argument("--profile-proj", type=int, choices=(0, 1, 2, 3), default=2)
     p.add_argument("--small-configs", action="store_true",
                    help="1B-shaped single projections (fused QKV, MLP) per call, L2-cold and warm")
     p.add_argument("--load-time", action="store_true",
@@ -487,6 +488,48 @@ def run_small_configs(a, dist):
                           "hbm_peak_gbs": peak, "hbm_peak_source": src, "projections": rows}), flush=True)
 
 
+def run_profile_case(a, dist):
+    """A small case for profilers: four calls on one ~31B-shaped projection
+    (--profile-proj: 0 fused QKV, 1 o_proj, 2 fused gate+up, 3 down),
+    alternating two seeded weight copies so no call finds its weights in L2.
+    --profile-case gemv: aq_gemv_nvfp4 with --m tokens on the register-decode
+    kernel (--kernel regdecode) or the block-scaled MMA path (--kernel mma);
+    --profile-case load: aq_reconstruct_quantize_nvfp4 of a rank-4 theta
+    bundle.  Prints one JSON line with the device status; not a timing."""
+    import torch
+    from nvfp4_block_scaled_aq_gb300 import aq, inputs
+    import __graft_entry__
+    __graft_entry__.build()
+    torch.cuda.set_device(dist.local)
+    device = torch.device("cuda", dist.local)
+    n, k = inputs.LAYER_31B[a.profile_proj]
+    qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+    if a.profile_case == "load":
+        th = inputs.theta(n, k, 4, seed=inputs.seed_of(9800), device=device)
+        w = aq.Nvfp4Weight.empty(n, k, device=device)
+        for _ in range(4):
+            aq.reconstruct_quantize(th.W0, th.s, th.U, th.V, w, qws)
+    else:
+        ws_w = []
+        for c in range(2):
+            W = inputs.weight(n, k, seed=inputs.seed_of(0, c, a.profile_proj), device=device)
+            w = aq.Nvfp4Weight.empty(n, k, device=device)
+            aq.quantize(W, w, qws)
+            ws_w.append(w)
+            del W
+        x = inputs.tokens(a.m, k, seed=inputs.seed_of(1, 0, a.profile_proj), device=device)
+        y = torch.empty((a.m, n), dtype=torch.bfloat16, device=device)
+        ws = torch.zeros(aq.gemv_workspace_bytes(n, k, a.m), dtype=torch.uint8, device=device)
+        path = aq.PATH_MMA if a.kernel == "mma" else aq.PATH_GEMV_REGDECODE
+        for i in range(4):
+            aq.gemv(ws_w[i % 2], x, y, ws, path=path)
+    torch.cuda.synchronize()
+    st = aq.poll_device_status()
+    if dist.rank == 0:
+        print(json.dumps({"profile_case": a.profile_case, "shape": [n, k], "m": a.m,
+                          "kernel": a.kernel, "status": st}), flush=True)
+
+
 def kernel_sha():
     h = hashlib.sha1()
     for name in ("gemv_core.cuh", "gemv.cu"):
@@ -626,6 +669,8 @@ def run_aq(a, dist):
     # graph, on the kernel chosen by --kernel (the library's default unless
     # asked otherwise: fixed, so a profiler's launch list sees the same legs)
     flags = {"regdecode": aq.STEP_REGDECODE, "tcgen05": aq.STEP_TCGEN05}
+    if a.kernel == "mma":  # the block-scaled MMA path, on request only
+        flags["mma"] = aq.STEP_MMA
     kernel = a.kernel
     kflag = flags[kernel]
     g_pdl = capture(stack, aq.STEP_PDL | kflag, stream)
@@ -700,7 +745,8 @@ def run_aq(a, dist):
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "peak_source": peak_kind + " (MEASURED_PEAKS.json hbm_gbs, copy burst)",
-                "kernel": ("gemv_kernel<1>" if kernel == "regdecode" else "tc_gemv_kernel") +
+                "kernel": {"regdecode": "gemv_kernel<1>", "tcgen05": "tc_gemv_kernel",
+                           "mma": "mma_gemm_kernel"}[kernel] +
                           " (aq_decode_step_weights: one launch per projection)",
                 "algorithmic_bytes_per_launch": round(launch_bytes)}
 
@@ -979,6 +1025,8 @@ def main():
             run_load_time(a, dist)
         elif a.small_configs:
             run_small_configs(a, dist)
+        elif a.profile_case:
+            run_profile_case(a, dist)
         else:
             run_aq(a, dist)
     finally:

@@ -18,7 +18,7 @@
 //  * each projection uses the partition and kernel form of the
 //    single-projection launch (the balanced stream-K grid, the one-token
 //    form for m = 1), so every output equals aq_gemv_nvfp4 on the
-//    register-decode kernel bit for bit;
+//    register-decode kernel bit for bit.
 //
 // The plan (device memory, written once by aq_step_plan_create) holds a
 // header and, per projection, the two tensor maps, the pointers and the
