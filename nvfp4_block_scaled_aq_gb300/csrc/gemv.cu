@@ -275,6 +275,26 @@ bool encode_bf16_map(const uint16_t *w, int n, int k, CUtensorMap *tm) {
   return cached_map(tm, w, uint64_t(k) * 2, uint64_t(n), kUnitCols, kRB, true);
 }
 
+// bf16 matrix [n, k] as bytes [n rows, 2k bytes]: boxes of 128 B (64
+// values) x box_rows rows with the 128-byte swizzle.
+bool encode_bf16_rows_map(const uint16_t *w, int n, int k, int box_rows, CUtensorMap *tm) {
+  if (!encoder()) return false;
+  return cached_map(tm, w, uint64_t(k) * 2, uint64_t(n), 128, uint32_t(box_rows), true);
+}
+
+// A byte array of `bytes` bytes as a 1-D tensor, copied in boxes of `box`
+// bytes; bytes past the end read as zero.
+bool encode_bytes_1d(const void *base, uint64_t bytes, uint32_t box, CUtensorMap *tm) {
+  if (!encoder()) return false;
+  const cuuint64_t dims[1] = {bytes};
+  const cuuint64_t strides[1] = {bytes};
+  const cuuint32_t boxd[1] = {box};
+  const cuuint32_t estr[1] = {1};
+  return g_encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, const_cast<void *>(base), dims, strides,
+                  boxd, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace core
 
 bool encode_act_maps(const uint8_t *xq, const uint8_t *xs, int m, int k, int scale_pitch,

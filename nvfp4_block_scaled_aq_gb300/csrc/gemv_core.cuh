@@ -1211,6 +1211,8 @@ size_t smem_bytes(int stages, int x_cap_halves, int rg);
 int stages_for(int x_cap_halves, int rg);
 bool encode_maps(const aq_nvfp4_weight &w, CUtensorMap *tm_w, CUtensorMap *tm_s, int rg);
 bool encode_bf16_map(const uint16_t *w, int n, int k, CUtensorMap *tm);
+bool encode_bf16_rows_map(const uint16_t *w, int n, int k, int box_rows, CUtensorMap *tm);
+bool encode_bytes_1d(const void *base, uint64_t bytes, uint32_t box, CUtensorMap *tm);
 
 }  // namespace core
 }  // namespace aq

@@ -12,7 +12,10 @@
 // Every fp32 step that decides a stored bit uses an explicitly rounded
 // intrinsic (__fmul_rn, __fdiv_rn, __fmaf_rn) so the compiler cannot fuse
 // or reorder it.
+#include <mutex>
+
 #include "aq_internal.cuh"
+#include "gemv_core.cuh"
 
 namespace aq {
 namespace {
@@ -169,31 +172,96 @@ __device__ __forceinline__ bool global_scales(uint32_t amax_bits, float &g_enc,
   return !isinf(g_enc);
 }
 
-// Quantise one 16-element block held as fp32 in w[0..15]: returns the E4M3
-// scale code and writes 8 packed bytes as two 32-bit words.
-__device__ __forceinline__ uint32_t quantize_block(const float *w, float g_enc,
-                                                   uint32_t &lo, uint32_t &hi) {
-  float b = 0.0f;
+// Two fp32 -> bf16x2 (nearest even), `hi` in the upper half.
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float hi, float lo) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ void unpack2(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// The bf16 pair w (element 0 in the low half) as an fp32 pair.
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+  return pack2(bf16_lo(w), bf16_hi(w));
+}
+
+// RN(b / 6) for a non-negative bf16 value b held as fp32: the product with
+// RN(1/6), corrected by one fma residual step.  For every such b (+0, the
+// subnormals, every finite normal; verified exhaustively) this is the
+// correctly rounded quotient, __fdiv_rn(b, 6.0f).
+__device__ __forceinline__ float div6_rn(float b) {
+  const float c = 0x1.555556p-3f;  // 1/6 rounded to nearest
+  const float q0 = __fmul_rn(b, c);
+  return __fmaf_rn(__fmaf_rn(-6.0f, q0, b), c, q0);
+}
+
+// rcp_tab[code] = RN(g_enc / decode(code)) for the E4M3 codes a block scale
+// can take (1 .. 0x7E; entry 0 unused).  The caller synchronises before the
+// first read.
+__device__ __forceinline__ void fill_rcp_table(float g_enc, float *rcp_tab) {
+  for (int i = threadIdx.x; i < 128; i += blockDim.x) {
+    const float sd = f16_lo_to_f32(e4m3x2_to_f16x2(uint16_t(i)));
+    rcp_tab[i] = i == 0 ? 0.0f : __fdiv_rn(g_enc, sd);
+  }
+}
+
+// Eight bf16 values (pairs w0 .. w3, element 2i in the low half of word i)
+// times rcp, each product rounded to fp32 and converted to E2M1 (nearest
+// even, saturated at 6, sign kept, also for a magnitude that rounds to
+// zero): one 32-bit word, element 2i in the low nibble of byte i.
+__device__ __forceinline__ uint32_t e2m1x8_scaled(uint32_t w0, uint32_t w1, uint32_t w2,
+                                                  uint32_t w3, uint64_t r2) {
+  const uint32_t w[4] = {w0, w1, w2, w3};
+  float p[8];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) b = fmaxf(b, fabsf(w[i]));
-  const float t = __fmul_rn(__fdiv_rn(b, 6.0f), g_enc);
+  for (int i = 0; i < 4; ++i) {
+    uint64_t v;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(v) : "l"(bf16x2_to_f32x2(w[i])), "l"(r2));
+    unpack2(v, p[2 * i], p[2 * i + 1]);
+  }
+  uint32_t out;
+  asm("{ .reg .b8 b0, b1, b2, b3;\n"
+      "  cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+      "  cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+      "  cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+      "  cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+      "  mov.b32 %0, {b0, b1, b2, b3}; }"
+      : "=r"(out)
+      : "f"(p[0]), "f"(p[1]), "f"(p[2]), "f"(p[3]), "f"(p[4]), "f"(p[5]), "f"(p[6]),
+        "f"(p[7]));
+  return out;
+}
+
+// Quantise one 16-element block given as eight bf16 pairs (element 2i in
+// the low half of bw[i]): returns the E4M3 scale code and writes the eight
+// packed bytes as two 32-bit words.  b = max |w| is the larger magnitude of
+// a max.xorsign.abs chain over the pairs (the sign it leaves is dropped);
+// sf = E4M3(RN(RN(b / 6) * g_enc)); if sf decodes to 0 (code 0) the nibbles
+// are 0, else nibble i = E2M1(RN(w_i * rcp_tab[sf])).
+__device__ __forceinline__ uint32_t quantize_block16(const uint32_t (&bw)[8], float g_enc,
+                                                     const float *__restrict__ rcp_tab,
+                                                     uint32_t &lo, uint32_t &hi) {
+  uint32_t m = bw[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) asm("max.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(bw[i]));
+  const uint32_t bb = max(m & 0x7FFFu, (m >> 16) & 0x7FFFu);
+  const float t = __fmul_rn(div6_rn(__uint_as_float(bb << 16)), g_enc);
   const uint32_t sf = f32x2_to_e4m3x2(0.0f, t) & 0xFFu;
-  const uint32_t sd_h2 = e4m3x2_to_f16x2(uint16_t(sf));
-  const float sd = f16_lo_to_f32(sd_h2);
   lo = hi = 0;
-  if (sd != 0.0f) {
-    const float rcp = __fdiv_rn(g_enc, sd);
-    uint32_t bytes[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const float v0 = __fmul_rn(w[2 * i], rcp);
-      const float v1 = __fmul_rn(w[2 * i + 1], rcp);
-      // the conversion keeps the sign, a negative value that rounds to zero
-      // included (nibble 0x8); the sweep over every bf16 value checks it
-      bytes[i] = f32x2_to_e2m1x2(v1, v0);
-    }
-    lo = bytes[0] | (bytes[1] << 8) | (bytes[2] << 16) | (bytes[3] << 24);
-    hi = bytes[4] | (bytes[5] << 8) | (bytes[6] << 16) | (bytes[7] << 24);
+  if (sf != 0) {
+    const float rcp = rcp_tab[sf];
+    const uint64_t r2 = pack2(rcp, rcp);
+    lo = e2m1x8_scaled(bw[0], bw[1], bw[2], bw[3], r2);
+    hi = e2m1x8_scaled(bw[4], bw[5], bw[6], bw[7], r2);
   }
   return sf;
 }
@@ -214,6 +282,9 @@ __global__ void __launch_bounds__(kThreads)
     *global_scale = ok ? g_dec : __int_as_float(0x7FC00000);
     if (!ok) raise_status(status, kDevRange);
   }
+  __shared__ float rcp_tab[128];
+  fill_rcp_table(g_enc, rcp_tab);
+  __syncthreads();
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int64_t tiles_k = ceil_div(k, kTileCols);
@@ -229,17 +300,15 @@ __global__ void __launch_bounds__(kThreads)
     for (int h = 0; h < 2; ++h) {
       const int64_t row = tn * kTileRows + 8 * h + g;
       if (row >= n || col >= k) continue;
-      float w[32];
+      uint32_t bw[2][8];  // the row's 32 values as bf16 pairs, per block
       if (!kFused) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint4 v = __ldg(reinterpret_cast<const uint4 *>(W + row * k + col) + q);
-          const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            w[8 * q + 2 * i] = bf16_lo(vv[i]);
-            w[8 * q + 2 * i + 1] = bf16_hi(vv[i]);
-          }
+          bw[q >> 1][4 * (q & 1)] = v.x;
+          bw[q >> 1][4 * (q & 1) + 1] = v.y;
+          bw[q >> 1][4 * (q & 1) + 2] = v.z;
+          bw[q >> 1][4 * (q & 1) + 3] = v.w;
         }
       } else {
         const float srow = __ldg(s + row);
@@ -254,16 +323,15 @@ __global__ void __launch_bounds__(kThreads)
             const int64_t j = col + 8 * q + 2 * i;
             const float lo = recon_elem<R>(bf16_lo(vv[i]), srow, u, V + j * rr, r);
             const float hi = recon_elem<R>(bf16_hi(vv[i]), srow, u, V + (j + 1) * rr, r);
-            w[8 * q + 2 * i] = __uint_as_float(uint32_t(f32_to_bf16_rn(lo)) << 16);
-            w[8 * q + 2 * i + 1] = __uint_as_float(uint32_t(f32_to_bf16_rn(hi)) << 16);
+            bw[q >> 1][4 * (q & 1) + i] = f32x2_to_bf16x2(hi, lo);
           }
         }
       }
       uint4 out = make_uint4(0, 0, 0, 0);
       uint32_t sf0 = 0, sf1 = 0;
       if (ok) {
-        sf0 = quantize_block(w, g_enc, out.x, out.y);
-        sf1 = quantize_block(w + 16, g_enc, out.z, out.w);
+        sf0 = quantize_block16(bw[0], g_enc, rcp_tab, out.x, out.y);
+        sf1 = quantize_block16(bw[1], g_enc, rcp_tab, out.z, out.w);
       }
       *reinterpret_cast<uint4 *>(packed + row * (k / 2) + col / 2) = out;
       sword |= (sf0 | (sf1 << 8)) << (16 * h);
@@ -272,199 +340,321 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// ---------------------------------------------------------- rank 4, V reused
-// The fused form for the configured rank (4) with V 16-byte aligned.  Each
-// warp keeps one 128-column tile column for its whole life and walks down
-// its row tiles (warps w and w + P * tiles_k share a tile column; P row
-// tiles are in flight per column), so the V rows it reads stay in L1; per
-// 16-column block lane (g, c) loads the block's V rows once (128 bytes,
-// eight 16-byte loads) and rebuilds rows g and g + 8 from them.  The
-// arithmetic is recon_elem<4>'s, in the same order.
+// ---------------------------------------------------------- rank 4, packed fp32
+// The fused form for the configured rank (4) with V 16-byte aligned.  The
+// eight warps of a CTA share one 128-column tile column and walk down its
+// row tiles, each warp its own sequence of them.  Lane 4g + c owns rows g
+// and g + 8 of each tile and columns [32c, 32c + 32): two 16-element blocks
+// per row, whose four E4M3 scales form the lane's word of the scale layout.
+//
+// The tile column's 128 columns of V sit in shared memory as fp32, rank-major
+// (vt[t][c][j] = V[col0 + 32c + j][t]), so one 16-byte shared load gives
+// rank entry t of four consecutive columns: two (column j, column j + 1)
+// pairs for the packed fp32 fma, which rebuilds two neighbouring elements of
+// a row per instruction.  Each chunk row is padded to 36 floats so that the
+// four chunks' loads fall in different banks.
+//
+// Arithmetic, element by element the operations of recon_elem<4>: the rank
+// term is an fma chain over t ascending from +0, run here on -u (an exact
+// negation), so it ends at m = -delta when delta != 0 and at m = +0 when
+// delta == 0 (round-to-nearest gives a zero sum the sign -0 only when both
+// addends are -0, and the chain starts at +0).  fma(s, w0, -m) is then
+// fma(s, w0, delta) when delta != 0, exact cancellation included, and
+// fma(s, w0, -0) = s * w0 rounded once, with the product's own sign of
+// zero, when delta == 0.  The amax pass needs only |e|, which the sign of a
+// zero does not change, so it takes fma(-s, w0, m) = -e on packed pairs.
+// The quantisation pass walks its row tiles in the reverse order, so that it
+// starts on the weights the amax pass read last, while they are still in L2.
 
-// One element of the rank-4 rebuild (fp32, before the bf16 rounding) from V
-// values already in registers: recon_elem<4>'s value.  The zero-delta case
-// (s * w0 alone) is one fma with -0 as the addend: fma(s, w0, -0) is the
-// product rounded once, -0 when the product is -0 and +0 when it is +0,
-// exactly as the rounded product itself.
-__device__ __forceinline__ float recon4(float w0, float s, const float (&u)[4], uint32_t v01,
-                                        uint32_t v23) {
-  float delta = 0.0f;
-  delta = __fmaf_rn(u[0], bf16_lo(v01), delta);
-  delta = __fmaf_rn(u[1], bf16_hi(v01), delta);
-  delta = __fmaf_rn(u[2], bf16_lo(v23), delta);
-  delta = __fmaf_rn(u[3], bf16_hi(v23), delta);
-  return __fmaf_rn(s, w0, delta == 0.0f ? -0.0f : delta);
+constexpr int kVtPitch = 36;                 // floats per (rank, chunk) row
+constexpr int kVtFloats = 4 * 4 * kVtPitch;  // one tile column's V tile
+
+// Element-wise a * b + c on fp32 pairs, each rounded once (fma.rn.f32).
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
 }
 
-// Two fp32 -> bf16x2 (nearest even), `hi` in the upper half.
-__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float hi, float lo) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
-// V rows of the 16 columns starting at col: column j's four entries in
-// vr[2j] (entries 0, 1) and vr[2j + 1] (entries 2, 3).
-__device__ __forceinline__ void load_v16(const uint16_t *__restrict__ V, int64_t col,
-                                         uint32_t (&vr)[32]) {
-  const uint4 *src = reinterpret_cast<const uint4 *>(V + col * 4);
+// Stage the tile column's V tile, negated (-v is exact, and fma(u, -v, m)
+// equals fma(-u, v, m)): lane l converts columns col0 + 4l .. + 3 (two
+// 16-byte loads of four bf16 rank entries per column); columns at or past k
+// are zero.
+__device__ __forceinline__ void stage_vt(const uint16_t *__restrict__ V, int64_t col0, int k,
+                                         int lane, float *vt) {
+  const int64_t cb = col0 + 4 * lane;
+  uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+  if (cb < k) {
+    a = __ldg(reinterpret_cast<const uint4 *>(V + cb * 4));
+    b = __ldg(reinterpret_cast<const uint4 *>(V + cb * 4) + 1);
+  }
+  // column cb + q, rank t: word (2q + t / 2) of (a, b), half t % 2
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  const int ch = lane >> 3, j = 4 * (lane & 7);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const uint4 v = __ldg(src + i);
-    vr[4 * i] = v.x;
-    vr[4 * i + 1] = v.y;
-    vr[4 * i + 2] = v.z;
-    vr[4 * i + 3] = v.w;
+  for (int t = 0; t < 4; ++t) {
+    float4 v;
+    v.x = -((t & 1) ? bf16_hi(w[0 + (t >> 1)]) : bf16_lo(w[0 + (t >> 1)]));
+    v.y = -((t & 1) ? bf16_hi(w[2 + (t >> 1)]) : bf16_lo(w[2 + (t >> 1)]));
+    v.z = -((t & 1) ? bf16_hi(w[4 + (t >> 1)]) : bf16_lo(w[4 + (t >> 1)]));
+    v.w = -((t & 1) ? bf16_hi(w[6 + (t >> 1)]) : bf16_lo(w[6 + (t >> 1)]));
+    *reinterpret_cast<float4 *>(vt + (t * 4 + ch) * kVtPitch + j) = v;
   }
 }
 
-// The 16 rebuilt values (bf16-rounded, as fp32) of row `row`, columns
-// col .. col + 15.
-__device__ __forceinline__ void rebuild16(const uint16_t *__restrict__ W0, float srow,
-                                          const float (&u)[4], int k, int64_t row, int64_t col,
-                                          const uint32_t (&vr)[32], float (&w)[16]) {
+
+// s and the U row (two bf16 pairs) of one row of a stage's tile.
+struct R4Row {
+  float s;
+  uint32_t u01, u23;
+};
+
+// The weights reach shared memory through a three-stage ring per warp: a
+// stage holds one row tile of the warp's tile column as two TMA boxes of 16
+// rows x 64 columns (128 bytes per row, 128-byte swizzle: 16-byte chunk j of
+// row r sits at chunk j ^ (r & 7)); rows past n and columns past k read as
+// zero.  The tile's 16 U rows (128 bytes) and 16 s values (64 bytes) come
+// with it, as 1-D boxes into a side buffer of the stage (zero past n).  Lane
+// 0 refills a stage once every lane of the warp has read it, so two row
+// tiles are in flight while the warp converts one.
+constexpr int kR4Stages = 2;
+constexpr int kR4BoxBytes = kTileRows * 128;    // one 16 x 64 box
+constexpr int kR4StageBytes = 2 * kR4BoxBytes;  // one row tile
+constexpr int kR4Warps = kThreads / 32;
+constexpr int kR4RowBytes = kTileRows * 8 + kTileRows * 4;  // U rows, then s
+constexpr int kR4RowStride = 256;  // side buffers 128-byte aligned for the TMA
+constexpr int kR4RingBytes = kR4Warps * kR4Stages * kR4StageBytes;
+constexpr int kR4RowsOffset = kR4RingBytes + kVtFloats * 4;
+constexpr int kR4BarsOffset = kR4RowsOffset + kR4Warps * kR4Stages * kR4RowStride;
+constexpr int kR4SmemBytes = 1024 + kR4BarsOffset + kR4Warps * kR4Stages * 8;
+
+static_assert(kR4RowsOffset % 128 == 0, "TMA side buffers must be 128-byte aligned");
+
+struct R4Maps {
+  CUtensorMap w0, u, s;
+};
+
+__device__ __forceinline__ void tma_load_1d(void *dst, const CUtensorMap *map, int x,
+                                            uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.1d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2}], [%3];" ::"r"(core::smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(core::smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void r4_issue(const R4Maps &tm, uint8_t *stage, uint8_t *rows,
+                                         uint64_t *bar, int64_t tn, int64_t col0, int k) {
+  const bool two = col0 + 64 < k;
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  core::mbar_expect_tx(bar, (two ? kR4StageBytes : kR4BoxBytes) + kR4RowBytes);
+  core::tma_load_2d(stage, &tm.w0, int(col0 * 2), int(tn * kTileRows), bar);
+  if (two)
+    core::tma_load_2d(stage + kR4BoxBytes, &tm.w0, int(col0 * 2 + 128), int(tn * kTileRows),
+                      bar);
+  tma_load_1d(rows, &tm.u, int(tn * kTileRows * 8), bar);
+  tma_load_1d(rows + kTileRows * 8, &tm.s, int(tn * kTileRows * 4), bar);
+}
+
+__device__ __forceinline__ R4Row r4_row(const uint8_t *rows, int r) {
+  const uint2 u = reinterpret_cast<const uint2 *>(rows)[r];
+  return R4Row{reinterpret_cast<const float *>(rows + kTileRows * 8)[r], u.x, u.y};
+}
+
+// Lane (g, c)'s 32 columns of rows g and g + 8 from a stage: w[h][q] holds
+// columns 8q .. 8q + 7 of the lane's chunk.  The four lanes of each bank
+// group differ in c, so each 16-byte load takes the minimum four wavefronts.
+__device__ __forceinline__ void r4_read(const uint8_t *stage, int g, int c, uint4 (&w)[2][4]) {
+  const uint8_t *box = stage + (c >> 1) * kR4BoxBytes;
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(W0 + row * k + col) + q);
-    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+  for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int j = 8 * q + 2 * i;
-      const float lo = recon4(bf16_lo(vv[i]), srow, u, vr[2 * j], vr[2 * j + 1]);
-      const float hi = recon4(bf16_hi(vv[i]), srow, u, vr[2 * j + 2], vr[2 * j + 3]);
-      const uint32_t b2 = f32x2_to_bf16x2(hi, lo);
-      w[j] = bf16_lo(b2);
-      w[j + 1] = bf16_hi(b2);
+    for (int q = 0; q < 4; ++q)
+      w[h][q] = *reinterpret_cast<const uint4 *>(box + (8 * h + g) * 128 +
+                                                 (((4 * (c & 1) + q) ^ g) << 4));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// One 16-column block (columns 16b .. 16b + 15 of the lane's chunk) of both
+// rows.  nu[h][t] = (u_t, u_t) of row h (see r4_pairs).  The amax pass folds |e| into mx
+// (NaN-propagating maximum); the quantisation pass writes the block's two
+// packed words per row into out[h][2b], out[h][2b + 1] and returns the four
+// scale codes' contribution to the lane's scale word.
+template <bool kQuant>
+__device__ __forceinline__ uint32_t r4_block(const uint4 (&w)[2][4], const R4Row (&rw)[2],
+                                             const uint64_t (&nu)[2][4],
+                                             const float *__restrict__ vc, int b, float g_enc,
+                                             const float *__restrict__ rcp_tab, bool ok,
+                                             float &mx, uint32_t (&out)[2][4]) {
+  uint32_t bw[2][8];
+#pragma unroll
+  for (int qd = 0; qd < 4; ++qd) {
+    uint64_t m[2][2] = {{0ull, 0ull}, {0ull, 0ull}};  // (+0, +0)
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(vc + t * 4 * kVtPitch +
+                                                                 16 * b + 4 * qd);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        m[h][0] = fma2(nu[h][t], v.x, m[h][0]);
+        m[h][1] = fma2(nu[h][t], v.y, m[h][1]);
+      }
     }
-  }
-}
-
-// max over the 16 values of |e| (fp32, before the bf16 rounding) as bit
-// patterns with the sign cleared, so a NaN or an infinity sorts above every
-// finite value.  Rounding to nearest is monotonic in magnitude, so the
-// largest |bf16(e)| is bf16 of the largest |e|: the caller rounds once.
-__device__ __forceinline__ uint32_t rebuild16_absmax(const uint16_t *__restrict__ W0, float srow,
-                                                     const float (&u)[4], int k, int64_t row,
-                                                     int64_t col, const uint32_t (&vr)[32],
-                                                     uint32_t m) {
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(W0 + row * k + col) + q);
-    const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+    for (int h = 0; h < 2; ++h) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int j = 8 * q + 2 * i;
-      const float lo = recon4(bf16_lo(vv[i]), srow, u, vr[2 * j], vr[2 * j + 1]);
-      const float hi = recon4(bf16_hi(vv[i]), srow, u, vr[2 * j + 2], vr[2 * j + 3]);
-      m = max(m, __float_as_uint(lo) & 0x7FFFFFFFu);
-      m = max(m, __float_as_uint(hi) & 0x7FFFFFFFu);
-    }
-  }
-  return m;
-}
-
-__device__ __forceinline__ void row_terms(const float *__restrict__ s,
-                                          const uint16_t *__restrict__ U, int64_t row,
-                                          float &srow, float (&u)[4]) {
-  srow = __ldg(s + row);
-#pragma unroll
-  for (int t = 0; t < 4; ++t) u[t] = __uint_as_float(uint32_t(__ldg(U + row * 4 + t)) << 16);
-}
-
-__global__ void __launch_bounds__(kThreads)
-    amax_r4_kernel(const uint16_t *__restrict__ W0, const float *__restrict__ s,
-                   const uint16_t *__restrict__ U, const uint16_t *__restrict__ V, int n,
-                   int k, int rows_in_flight, uint32_t *amax_bits) {
-  const int lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
-  const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
-  const int64_t warp = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
-  uint32_t m = 0;
-  if (warp < tiles_k * rows_in_flight) {
-    const int64_t tk = warp % tiles_k, tn0 = warp / tiles_k;
-    const int64_t col = tk * kTileCols + 32 * c;
-    if (col < k)
-      for (int64_t tn = tn0; tn < tiles_n; tn += rows_in_flight) {
-        float srow[2], u[2][4];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int64_t row = tn * kTileRows + 8 * h + g;
-          if (row < n) row_terms(s, U, row, srow[h], u[h]);
-        }
-#pragma unroll
-        for (int b = 0; b < 2; ++b) {
-          uint32_t vr[32];
-          load_v16(V, col + 16 * b, vr);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t row = tn * kTileRows + 8 * h + g;
-            if (row >= n) continue;
-            m = rebuild16_absmax(W0, srow[h], u[h], k, row, col + 16 * b, vr, m);
-          }
+      for (int p = 0; p < 2; ++p) {
+        const int pi = 2 * qd + p;  // column pair within the block
+        const uint32_t wd = word_of(w[h][2 * b + (pi >> 2)], pi & 3);
+        if (kQuant) {
+          float mlo, mhi;
+          unpack2(m[h][p], mlo, mhi);
+          const float elo = __fmaf_rn(rw[h].s, bf16_lo(wd), -mlo);
+          const float ehi = __fmaf_rn(rw[h].s, bf16_hi(wd), -mhi);
+          bw[h][pi] = f32x2_to_bf16x2(ehi, elo);
+        } else {
+          const uint64_t e = fma2(pack2(-rw[h].s, -rw[h].s), bf16x2_to_f32x2(wd), m[h][p]);
+          float elo, ehi;
+          unpack2(e, elo, ehi);
+          asm("max.NaN.abs.f32 %0, %0, %1, %2;" : "+f"(mx) : "f"(elo), "f"(ehi));
         }
       }
+    }
   }
-  // bf16 bits of the largest |e|: a NaN stays a NaN pattern and an
-  // infinity the infinity pattern, both at or above 0x7F80
-  uint32_t mb = m >= 0x7F800000u ? (m >> 16) | (m > 0x7F800000u ? 0x40u : 0u)
-                                 : uint32_t(f32_to_bf16_rn(__uint_as_float(m)));
-  mb = block_max_u32(mb);
-  if (threadIdx.x == 0) atomicMax(amax_bits, mb);
+  uint32_t sword = 0;
+  if (kQuant) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t sf = 0;
+      out[h][2 * b] = out[h][2 * b + 1] = 0;
+      if (ok) sf = quantize_block16(bw[h], g_enc, rcp_tab, out[h][2 * b], out[h][2 * b + 1]);
+      sword |= sf << (16 * h + 8 * b);
+    }
+  }
+  return sword;
 }
 
-__global__ void __launch_bounds__(kThreads)
-    quantize_r4_kernel(const uint16_t *__restrict__ W0, const float *__restrict__ s,
-                       const uint16_t *__restrict__ U, const uint16_t *__restrict__ V, int n,
-                       int k, int rows_in_flight, uint8_t *__restrict__ packed,
-                       uint8_t *__restrict__ scales, float *__restrict__ global_scale,
-                       const uint32_t *__restrict__ amax_bits, unsigned *status) {
-  float g_enc = 1.0f, g_dec = 1.0f;
-  const bool ok = global_scales(*amax_bits, g_enc, g_dec);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    *global_scale = ok ? g_dec : __int_as_float(0x7FC00000);
-    if (!ok) raise_status(status, kDevRange);
+// nu[h][t] = (u_t, u_t) of row h: the chain runs on u against the negated
+// V tile, i.e. on -u against V.
+__device__ __forceinline__ void r4_pairs(const R4Row (&rw)[2], uint64_t (&nu)[2][4]) {
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float u[4] = {bf16_lo(rw[h].u01), bf16_hi(rw[h].u01), bf16_lo(rw[h].u23),
+                        bf16_hi(rw[h].u23)};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) nu[h][t] = pack2(u[t], u[t]);
   }
-  const int lane = threadIdx.x & 31;
-  const int g = lane >> 2, c = lane & 3;
+}
+
+// kQuant = false: the amax pass (max |e| over the tensor into *amax_bits as
+// bf16 bits, like amax_kernel); kQuant = true: the quantisation pass.  Each
+// warp runs its own weight ring (see r4_issue) and loads the next tile's s
+// and U rows while it converts the current one.  A ring wait that gives up
+// raises kDevTimeout, waits (bounded) for the warp's other copies in flight
+// and ends the warp's work.
+template <bool kQuant>
+__global__ void __launch_bounds__(kThreads, 2)
+    recon_r4_kernel(const __grid_constant__ R4Maps tm, const uint16_t *__restrict__ V, int n,
+                    int k, int ctas_per_col, uint8_t *__restrict__ packed,
+                    uint8_t *__restrict__ scales, float *__restrict__ global_scale,
+                    uint32_t *amax_bits, unsigned *status) {
+  extern __shared__ uint8_t r4_smem_raw[];
+  __shared__ float rcp_tab[128];
+  __shared__ int never;  // abort flag of the bounded waits; nothing sets it
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(r4_smem_raw) + 1023) & ~uintptr_t(1023));
+  const int wi = threadIdx.x >> 5;
+  uint8_t *ring = smem + wi * kR4Stages * kR4StageBytes;
+  float *vt = reinterpret_cast<float *>(smem + kR4RingBytes);
+  uint8_t *rows = smem + kR4RowsOffset + wi * kR4Stages * kR4RowStride;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kR4BarsOffset) + wi * kR4Stages;
+  if (threadIdx.x == 0) never = 0;
+  float g_enc = 1.0f;
+  bool ok = true;
+  if (kQuant) {
+    float g_dec = 1.0f;
+    ok = global_scales(*amax_bits, g_enc, g_dec);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+      *global_scale = ok ? g_dec : __int_as_float(0x7FC00000);
+      if (!ok) raise_status(status, kDevRange);
+    }
+    fill_rcp_table(g_enc, rcp_tab);
+  }
+  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
   const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
-  const int64_t warp = (blockIdx.x * int64_t(blockDim.x) + threadIdx.x) >> 5;
-  if (warp >= tiles_k * rows_in_flight) return;
-  const int64_t tk = warp % tiles_k, tn0 = warp / tiles_k;
-  const int64_t col = tk * kTileCols + 32 * c;
-  for (int64_t tn = tn0; tn < tiles_n; tn += rows_in_flight) {
-    float srow[2], u[2][4];
-    uint32_t out[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+  const int64_t tk = blockIdx.x % tiles_k;
+  const int64_t col0 = tk * kTileCols, col = col0 + 32 * c;
+  if (wi == 0) stage_vt(V, col0, k, lane, vt);
+  __syncthreads();
+  const int64_t rows_in_flight = int64_t(ctas_per_col) * kR4Warps;
+  const int64_t tn0 = (blockIdx.x / tiles_k) * kR4Warps + wi;
+  float mx = 0.0f;
+  const bool live = col < k;
+  const int64_t iters = tn0 < tiles_n ? ceil_div(tiles_n - tn0, rows_in_flight) : 0;
+  auto tile_of = [&](int64_t it) {
+    return tn0 + (kQuant ? iters - 1 - it : it) * rows_in_flight;
+  };
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < kR4Stages; ++st) core::mbar_init(&bars[st], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int d = 0; d < kR4Stages && d < iters; ++d)
+      r4_issue(tm, ring + d * kR4StageBytes, rows + d * kR4RowStride, &bars[d], tile_of(d),
+               col0, k);
+  }
+  __syncwarp();
+  const float *vc = vt + c * kVtPitch;
+  for (int64_t it = 0; it < iters; ++it) {
+    const int64_t tn = tile_of(it);
+    const int st = int(it % kR4Stages);
+    const bool arrived =
+        core::mbar_wait(&bars[st], unsigned(it / kR4Stages) & 1u, &never);
+    if (!__all_sync(0xFFFFFFFFu, arrived)) {
+      if (lane == 0) {
+        raise_status(status, kDevTimeout);
+        for (int64_t j = it + 1; j < it + kR4Stages && j < iters; ++j)
+          core::mbar_wait(&bars[j % kR4Stages], unsigned(j / kR4Stages) & 1u, &never);
+      }
+      break;
+    }
+    uint4 w[2][4];
+    r4_read(ring + st * kR4StageBytes, g, c, w);
+    const R4Row rw[2] = {r4_row(rows + st * kR4RowStride, g),
+                         r4_row(rows + st * kR4RowStride, 8 + g)};
+    __syncwarp();
+    if (lane == 0 && it + kR4Stages < iters)
+      r4_issue(tm, ring + st * kR4StageBytes, rows + st * kR4RowStride, &bars[st],
+               tile_of(it + kR4Stages), col0, k);
     uint32_t sword = 0;
-    if (col < k) {
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t row = tn * kTileRows + 8 * h + g;
-        if (row < n) row_terms(s, U, row, srow[h], u[h]);
-      }
-#pragma unroll
-      for (int b = 0; b < 2; ++b) {
-        uint32_t vr[32];
-        load_v16(V, col + 16 * b, vr);
+    if (live) {
+      uint64_t nu[2][4];
+      r4_pairs(rw, nu);
+      uint32_t out[2][4];
+      sword |= r4_block<kQuant>(w, rw, nu, vc, 0, g_enc, rcp_tab, ok, mx, out);
+      sword |= r4_block<kQuant>(w, rw, nu, vc, 1, g_enc, rcp_tab, ok, mx, out);
+      if (kQuant) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int64_t row = tn * kTileRows + 8 * h + g;
-          if (row >= n) continue;
-          float w[16];
-          rebuild16(W0, srow[h], u[h], k, row, col + 16 * b, vr, w);
-          uint32_t sf = 0;
-          if (ok) sf = quantize_block(w, g_enc, out[h][2 * b], out[h][2 * b + 1]);
-          sword |= sf << (16 * h + 8 * b);
+          if (row < n)
+            *reinterpret_cast<uint4 *>(packed + row * (k / 2) + col / 2) =
+                make_uint4(out[h][0], out[h][1], out[h][2], out[h][3]);
         }
       }
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t row = tn * kTileRows + 8 * h + g;
-        if (row < n)
-          *reinterpret_cast<uint4 *>(packed + row * (k / 2) + col / 2) =
-              make_uint4(out[h][0], out[h][1], out[h][2], out[h][3]);
-      }
     }
-    reinterpret_cast<uint32_t *>(scales + (tn * tiles_k + tk) * 128)[lane] = sword;
+    if (kQuant) reinterpret_cast<uint32_t *>(scales + (tn * tiles_k + tk) * 128)[lane] = sword;
+  }
+  if (!kQuant) {
+    // bf16 bits of the largest |e|: a NaN stays a NaN pattern and an
+    // infinity the infinity pattern, both at or above 0x7F80
+    const uint32_t m = __float_as_uint(mx);
+    uint32_t mb = m >= 0x7F800000u ? (m >> 16) | (m > 0x7F800000u ? 0x40u : 0u)
+                                   : uint32_t(f32_to_bf16_rn(mx));
+    mb = block_max_u32(mb);
+    if (threadIdx.x == 0) atomicMax(amax_bits, mb);
   }
 }
 
@@ -497,20 +687,15 @@ __global__ void __launch_bounds__(kThreads)
     g_dec[row] = ok ? gd : __int_as_float(0x7FC00000);
     if (!ok) raise_status(status, kDevRange);
   }
+  __shared__ float rcp_tab[128];
+  fill_rcp_table(g_enc, rcp_tab);
+  __syncthreads();
   for (int b = threadIdx.x; b < k / kBlock; b += kThreads) {
-    float w[16];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4 *>(xr + b * kBlock) + q);
-      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        w[8 * q + 2 * i] = bf16_lo(vv[i]);
-        w[8 * q + 2 * i + 1] = bf16_hi(vv[i]);
-      }
-    }
+    const uint4 v0 = __ldg(reinterpret_cast<const uint4 *>(xr + b * kBlock));
+    const uint4 v1 = __ldg(reinterpret_cast<const uint4 *>(xr + b * kBlock) + 1);
+    const uint32_t bw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     uint32_t lo = 0, hi = 0, sf = 0;
-    if (ok) sf = quantize_block(w, g_enc, lo, hi);
+    if (ok) sf = quantize_block16(bw, g_enc, rcp_tab, lo, hi);
     *reinterpret_cast<uint2 *>(packed + row * (k / 2) + b * 8) = make_uint2(lo, hi);
     scales[row * scale_pitch + b] = uint8_t(sf);
   }
@@ -569,20 +754,44 @@ static void quantize_pass(const uint16_t *W, const float *s, const uint16_t *U,
                                                      dev.status);
 }
 
-// Rank 4 with V reused per warp: P row tiles in flight per tile column,
-// about sixteen warps per SM in all (two CTAs of eight, one wave).
-static void quantize_pass_r4(const uint16_t *W, const float *s, const uint16_t *U,
-                             const uint16_t *V, int n, int k, const aq_nvfp4_weight &out,
-                             uint32_t *amax, const DeviceInfo &dev, cudaStream_t st) {
+// Rank 4: CTA j works tile column j % tiles_k with its eight warps on row
+// tiles 8 (j / tiles_k) + w + 8 Q i (Q CTAs per tile column), at most two
+// CTAs per SM in one wave.
+template <bool kQuant>
+static cudaError_t r4_smem_attr(int device) {
+  static bool done[64] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(
+      recon_r4_kernel<kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize, kR4SmemBytes);
+  if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
+  return e;
+}
+
+static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uint16_t *U,
+                                    const uint16_t *V, int n, int k,
+                                    const aq_nvfp4_weight &out, uint32_t *amax,
+                                    const DeviceInfo &dev, cudaStream_t st) {
+  R4Maps tm;
+  if (!core::encode_bf16_rows_map(W, n, k, kTileRows, &tm.w0) ||
+      !core::encode_bytes_1d(U, uint64_t(n) * 8, kTileRows * 8, &tm.u) ||
+      !core::encode_bytes_1d(s, uint64_t(n) * 4, kTileRows * 4, &tm.s))
+    return cudaErrorInvalidValue;
+  cudaError_t e = r4_smem_attr<false>(dev.ordinal);
+  if (e == cudaSuccess) e = r4_smem_attr<true>(dev.ordinal);
+  if (e != cudaSuccess) return e;
   const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
-  int64_t P = int64_t(dev.sms) * 16 / tiles_k;
-  if (P < 1) P = 1;
-  if (P > tiles_n) P = tiles_n;
-  const int warps_per_cta = kThreads / 32;
-  const int g = int(ceil_div(tiles_k * P, warps_per_cta));
-  amax_r4_kernel<<<g, kThreads, 0, st>>>(W, s, U, V, n, k, int(P), amax);
-  quantize_r4_kernel<<<g, kThreads, 0, st>>>(W, s, U, V, n, k, int(P), out.packed, out.scales,
-                                             out.global_scale, amax, dev.status);
+  int64_t Q = int64_t(dev.sms) * 2 / tiles_k;
+  if (Q > ceil_div(tiles_n, kR4Warps)) Q = ceil_div(tiles_n, kR4Warps);
+  if (Q < 1) Q = 1;
+  const int g = int(tiles_k * Q);
+  recon_r4_kernel<false><<<g, kThreads, kR4SmemBytes, st>>>(tm, V, n, k, int(Q), nullptr,
+                                                           nullptr, nullptr, amax, dev.status);
+  recon_r4_kernel<true><<<g, kThreads, kR4SmemBytes, st>>>(tm, V, n, k, int(Q), out.packed,
+                                                          out.scales, out.global_scale, amax,
+                                                          dev.status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U,
@@ -594,8 +803,9 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
   if (e != cudaSuccess) return e;
   if (!fused)
     quantize_pass<0, false>(W, s, U, V, 0, n, k, out, amax, dev, st);
-  else if (r == 4 && (reinterpret_cast<uintptr_t>(V) & 15u) == 0)
-    quantize_pass_r4(W, s, U, V, n, k, out, amax, dev, st);
+  else if (r == 4 && ((reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(U) |
+                        reinterpret_cast<uintptr_t>(s)) & 15u) == 0)
+    return quantize_pass_r4(W, s, U, V, n, k, out, amax, dev, st);
   else if (r == 0)
     quantize_pass<0, true>(W, s, U, V, r, n, k, out, amax, dev, st);
   else if (r == 4 && (reinterpret_cast<uintptr_t>(V) & 7u) == 0)

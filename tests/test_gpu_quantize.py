@@ -188,8 +188,8 @@ def test_rank4_v_alignment_paths_bit_exact(offset):
     """A rank-4 V that is only 2-byte aligned (a view one bf16 into a larger
     buffer) takes the generic rank path of the reconstruction and the fused
     reconstruct-and-quantise; one that is 8- but not 16-byte aligned (four
-    bf16 in) takes the per-element rank-4 path instead of the one that keeps
-    V rows in registers.  Every path stays bit-exact with the oracle."""
+    bf16 in) takes the per-element rank-4 path instead of the one that stages
+    V in shared memory.  Every path stays bit-exact with the oracle."""
     n, k, r = 48, 160, 4
     th = inputs.theta(n, k, r, seed=77, device=DEV)
     big = torch.empty(k * r + 8, dtype=torch.bfloat16, device=DEV)
@@ -205,3 +205,122 @@ def test_rank4_v_alignment_paths_bit_exact(offset):
     aq.reconstruct_quantize(th.W0, th.s, th.U, V, w, ws)
     assert_quantized_equal(w, ref)
     assert aq.poll_device_status() == aq.OK
+
+
+@pytest.mark.parametrize("which", ["U", "s"])
+def test_rank4_u_s_alignment_fallback_bit_exact(which):
+    """The rank-4 path that streams the tile's U rows and s values by TMA
+    needs U and s 16-byte aligned; a U or an s view that is only naturally
+    aligned takes the per-element rank path and stays bit-exact."""
+    n, k, r = 48, 160, 4
+    th = inputs.theta(n, k, r, seed=78, device=DEV)
+    U, s = th.U, th.s
+    if which == "U":
+        big = torch.empty(n * r + 8, dtype=torch.bfloat16, device=DEV)
+        U = big[1:1 + n * r].view(n, r)
+        U.copy_(th.U)
+        assert U.data_ptr() % 16 == 2
+    else:
+        big = torch.empty(n + 4, dtype=torch.float32, device=DEV)
+        s = big[1:1 + n]
+        s.copy_(th.s)
+        assert s.data_ptr() % 16 == 4
+    ref = oracle.reconstruct(bits(th.W0), th.s.cpu().numpy(), bits(th.U), bits(th.V))
+    w = aq.Nvfp4Weight.empty(n, k, device=DEV)
+    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    aq.reconstruct_quantize(th.W0, s, U, th.V, w, ws)
+    assert_quantized_equal(w, ref)
+    assert aq.poll_device_status() == aq.OK
+
+
+def _fused_r4(W0b, s, Ub, Vb):
+    n, k = W0b.shape
+    w = aq.Nvfp4Weight.empty(n, k, device=DEV)
+    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    aq.reconstruct_quantize(to_dev(W0b), torch.as_tensor(s, device=DEV), to_dev(Ub),
+                            to_dev(Vb), w, ws)
+    return w
+
+
+@pytest.mark.parametrize("n,k", [(1, 32), (45, 160), (17, 4128), (300, 1152)])
+def test_rank4_packed_path_ragged_shapes_bit_exact(n, k):
+    """The rank-4 path with V 16-byte aligned on row counts that end inside a
+    16-row tile and widths that end inside a 128-column tile column."""
+    th = inputs.theta(n, k, 4, seed=n * 7 + k, device=DEV)
+    assert th.V.data_ptr() % 16 == 0
+    w = aq.Nvfp4Weight.empty(n, k, device=DEV)
+    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    aq.reconstruct_quantize(th.W0, th.s, th.U, th.V, w, ws)
+    ref = oracle.reconstruct(bits(th.W0), th.s.cpu().numpy(), bits(th.U), bits(th.V))
+    assert_quantized_equal(w, ref)
+    assert aq.poll_device_status() == aq.OK
+
+
+def test_rank4_zero_signs_and_exact_cancellation_bit_exact():
+    """AttnQuant docs, landing page, "How it works": W_eff = s*W0 + U*V^T,
+    with the rank term zero handled as s*W0 alone.  Rows built so that
+    (a) s*w0 + delta cancels exactly (the result is +0), (b) delta is zero
+    through an exact cancellation inside the rank sum, with s < 0 and signed
+    zeros in W0 (the product's sign of zero must survive), (c) U = 0 with
+    s = -0, +0 and negative s, (d) generic rows.  Every block also holds
+    non-zero values, so a zero's sign shows in its nibble (0x0 or 0x8)."""
+    rng = np.random.default_rng(5)
+    n, k = 64, 256
+    x = bf16_of(rng.normal(0, 0.05, k))            # shared row pattern
+    W0 = np.tile(bf16_of(rng.normal(0, 0.05, k)), (n, 1))
+    W0[:16, 0::2] = x[0::2]                         # (a) cancels with V[:, 0]
+    zero_mask = rng.random((n, k)) < 0.3
+    signs = np.where(rng.random((n, k)) < 0.5, 0x8000, 0x0000).astype(np.uint16)
+    W0[16:48][zero_mask[16:48]] = signs[16:48][zero_mask[16:48]]
+    W0[48:] = bf16_of(rng.normal(0, 0.05, (16, k)))
+    V = np.zeros((k, 4), np.uint16)
+    V[:, 0] = x ^ 0x8000                            # -x
+    V[:, 1] = x                                     # v0 + v1 = 0 exactly
+    V[:, 2] = bf16_of(rng.normal(0, 0.01, k))
+    V[:, 3] = bf16_of(rng.normal(0, 0.01, k))
+    one = bf16_of([1.0])[0]
+    U = np.zeros((n, 4), np.uint16)
+    U[:16, 0] = one                                 # (a) delta = -x_j
+    U[16:32, 0] = one
+    U[16:32, 1] = one                               # (b) delta = +0 by cancellation
+    U[48:] = bf16_of(rng.normal(0, 0.01, (16, 4)))  # (d)
+    s = np.exp(0.1 * rng.normal(size=n)).astype(np.float32)
+    s[:16] = 1.0
+    s[16:32] *= -1.5
+    s[32:36] = -0.0                                 # (c)
+    s[36:40] = 0.0
+    s[40:48] *= -1.0
+    w = _fused_r4(W0, s, U, V)
+    ref = oracle.reconstruct(W0, s, U, V)
+    assert np.all(ref[:16, 0::2] == 0)              # +0 from exact cancellation
+    neg_zero = (ref[16:48] == 0x8000).sum()
+    assert neg_zero > 100 and (ref[16:48] == 0).sum() > 100
+    assert_quantized_equal(w, ref)
+    assert aq.poll_device_status() == aq.OK
+
+
+@pytest.mark.parametrize("case", ["inf_in_w0", "inf_from_rank_term", "nan_in_v"])
+def test_rank4_non_finite_w_eff_sets_status(case):
+    """A non-finite W_eff on the rank-4 path is caught like a non-finite
+    weight: zero-filled outputs, NaN global scale, AQ_ERR_RANGE.  The rank
+    term can overflow to inf from finite inputs (the product inside an fma is
+    exact, so it cannot make a NaN); a NaN in one V entry makes one column of
+    W_eff NaN, which the amax pass must propagate past every finite value."""
+    rng = np.random.default_rng(9)
+    n, k = 32, 256
+    W0 = bf16_of(rng.normal(0, 0.02, (n, k)))
+    U = bf16_of(rng.normal(0, 0.01, (n, 4)))
+    V = bf16_of(rng.normal(0, 0.01, (k, 4)))
+    s = np.ones(n, np.float32)
+    if case == "inf_in_w0":
+        W0[5, 77] = 0x7F80
+    elif case == "inf_from_rank_term":
+        big = bf16_of([3.0e38])[0]
+        U[9] = [big, 0, 0, 0]
+        V[130, 0] = big
+    else:
+        V[201, 2] = 0x7FC0
+    w = _fused_r4(W0, s, U, V)
+    assert aq.poll_device_status() == aq.ERR_RANGE
+    gp, gs, gd = weight_bytes(w)
+    assert not gp.any() and not gs.any() and np.isnan(gd)
