@@ -341,13 +341,16 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------- rank 4, packed fp32
-// The fused form for the configured rank (4) with V 16-byte aligned.  The
-// eight warps of a CTA share one 128-column tile column and walk down its
-// row tiles, each warp its own sequence of them.  Lane 4g + c owns rows g
-// and g + 8 of each tile and columns [32c, 32c + 32): two 16-element blocks
-// per row, whose four E4M3 scales form the lane's word of the scale layout.
+// The fused form for the configured rank (4) with V 16-byte aligned.  Warp w
+// of W works tile column w % tiles_k, whose W_c warps (W / tiles_k, one more
+// for the first W % tiles_k columns) take its row tiles in turn; the eight
+// warps of a CTA hold neighbouring tile columns, so a CTA reads 16-row bands
+// of up to 2 KB per row.  Lane
+// 4g + c owns rows g and g + 8 of each tile and columns [32c, 32c + 32): two
+// 16-element blocks per row, whose four E4M3 scales form the lane's word of
+// the scale layout.
 //
-// The tile column's 128 columns of V sit in shared memory as fp32, rank-major
+// The warp's 128 columns of V sit in shared memory as fp32, rank-major
 // (vt[t][c][j] = V[col0 + 32c + j][t]), so one 16-byte shared load gives
 // rank entry t of four consecutive columns: two (column j, column j + 1)
 // pairs for the packed fp32 fma, which rebuilds two neighbouring elements of
@@ -367,7 +370,7 @@ __global__ void __launch_bounds__(kThreads)
 // starts on the weights the amax pass read last, while they are still in L2.
 
 constexpr int kVtPitch = 36;                 // floats per (rank, chunk) row
-constexpr int kVtFloats = 4 * 4 * kVtPitch;  // one tile column's V tile
+constexpr int kVtFloats = 4 * 4 * kVtPitch;  // one warp's V tile
 
 // Element-wise a * b + c on fp32 pairs, each rounded once (fma.rn.f32).
 __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
@@ -376,7 +379,7 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
   return d;
 }
 
-// Stage the tile column's V tile, negated (-v is exact, and fma(u, -v, m)
+// Stage the warp's V tile, negated (-v is exact, and fma(u, -v, m)
 // equals fma(-u, v, m)): lane l converts columns col0 + 4l .. + 3 (two
 // 16-byte loads of four bf16 rank entries per column); columns at or past k
 // are zero.
@@ -424,7 +427,7 @@ constexpr int kR4Warps = kThreads / 32;
 constexpr int kR4RowBytes = kTileRows * 8 + kTileRows * 4;  // U rows, then s
 constexpr int kR4RowStride = 256;  // side buffers 128-byte aligned for the TMA
 constexpr int kR4RingBytes = kR4Warps * kR4Stages * kR4StageBytes;
-constexpr int kR4RowsOffset = kR4RingBytes + kVtFloats * 4;
+constexpr int kR4RowsOffset = kR4RingBytes + kR4Warps * kVtFloats * 4;
 constexpr int kR4BarsOffset = kR4RowsOffset + kR4Warps * kR4Stages * kR4RowStride;
 constexpr int kR4SmemBytes = 1024 + kR4BarsOffset + kR4Warps * kR4Stages * 8;
 
@@ -490,25 +493,30 @@ __device__ __forceinline__ uint32_t r4_block(const uint4 (&w)[2][4], const R4Row
                                              const float *__restrict__ rcp_tab, bool ok,
                                              float &mx, uint32_t (&out)[2][4]) {
   uint32_t bw[2][8];
+  // Half a block (8 columns, 4 pairs) of both rows at a time, rank-outer:
+  // eight independent fma chains per rank step.
 #pragma unroll
-  for (int qd = 0; qd < 4; ++qd) {
-    uint64_t m[2][2] = {{0ull, 0ull}, {0ull, 0ull}};  // (+0, +0)
+  for (int hb = 0; hb < 2; ++hb) {
+    uint64_t m[2][4] = {{0ull, 0ull, 0ull, 0ull}, {0ull, 0ull, 0ull, 0ull}};  // (+0, +0)
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const ulonglong2 v = *reinterpret_cast<const ulonglong2 *>(vc + t * 4 * kVtPitch +
-                                                                 16 * b + 4 * qd);
+      const float *vr = vc + t * 4 * kVtPitch + 16 * b + 8 * hb;
+      const ulonglong2 va = *reinterpret_cast<const ulonglong2 *>(vr);
+      const ulonglong2 vb = *reinterpret_cast<const ulonglong2 *>(vr + 4);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        m[h][0] = fma2(nu[h][t], v.x, m[h][0]);
-        m[h][1] = fma2(nu[h][t], v.y, m[h][1]);
+        m[h][0] = fma2(nu[h][t], va.x, m[h][0]);
+        m[h][1] = fma2(nu[h][t], va.y, m[h][1]);
+        m[h][2] = fma2(nu[h][t], vb.x, m[h][2]);
+        m[h][3] = fma2(nu[h][t], vb.y, m[h][3]);
       }
     }
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
 #pragma unroll
-      for (int p = 0; p < 2; ++p) {
-        const int pi = 2 * qd + p;  // column pair within the block
-        const uint32_t wd = word_of(w[h][2 * b + (pi >> 2)], pi & 3);
+      for (int p = 0; p < 4; ++p) {
+        const int pi = 4 * hb + p;  // column pair within the block
+        const uint32_t wd = word_of(w[h][2 * b + hb], p);
         if (kQuant) {
           float mlo, mhi;
           unpack2(m[h][p], mlo, mhi);
@@ -549,85 +557,69 @@ __device__ __forceinline__ void r4_pairs(const R4Row (&rw)[2], uint64_t (&nu)[2]
   }
 }
 
-// kQuant = false: the amax pass (max |e| over the tensor into *amax_bits as
-// bf16 bits, like amax_kernel); kQuant = true: the quantisation pass.  Each
-// warp runs its own weight ring (see r4_issue) and loads the next tile's s
-// and U rows while it converts the current one.  A ring wait that gives up
-// raises kDevTimeout, waits (bounded) for the warp's other copies in flight
-// and ends the warp's work.
-template <bool kQuant>
-__global__ void __launch_bounds__(kThreads, 2)
-    recon_r4_kernel(const __grid_constant__ R4Maps tm, const uint16_t *__restrict__ V, int n,
-                    int k, int ctas_per_col, uint8_t *__restrict__ packed,
-                    uint8_t *__restrict__ scales, float *__restrict__ global_scale,
-                    uint32_t *amax_bits, unsigned *status) {
-  extern __shared__ uint8_t r4_smem_raw[];
-  __shared__ float rcp_tab[128];
-  __shared__ int never;  // abort flag of the bounded waits; nothing sets it
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(r4_smem_raw) + 1023) & ~uintptr_t(1023));
-  const int wi = threadIdx.x >> 5;
-  uint8_t *ring = smem + wi * kR4Stages * kR4StageBytes;
-  float *vt = reinterpret_cast<float *>(smem + kR4RingBytes);
-  uint8_t *rows = smem + kR4RowsOffset + wi * kR4Stages * kR4RowStride;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kR4BarsOffset) + wi * kR4Stages;
-  if (threadIdx.x == 0) never = 0;
-  float g_enc = 1.0f;
-  bool ok = true;
-  if (kQuant) {
-    float g_dec = 1.0f;
-    ok = global_scales(*amax_bits, g_enc, g_dec);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      *global_scale = ok ? g_dec : __int_as_float(0x7FC00000);
-      if (!ok) raise_status(status, kDevRange);
-    }
-    fill_rcp_table(g_enc, rcp_tab);
-  }
-  const int lane = threadIdx.x & 31, g = lane >> 2, c = lane & 3;
-  const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
-  const int64_t tk = blockIdx.x % tiles_k;
-  const int64_t col0 = tk * kTileCols, col = col0 + 32 * c;
-  if (wi == 0) stage_vt(V, col0, k, lane, vt);
-  __syncthreads();
-  const int64_t rows_in_flight = int64_t(ctas_per_col) * kR4Warps;
-  const int64_t tn0 = (blockIdx.x / tiles_k) * kR4Warps + wi;
-  float mx = 0.0f;
-  const bool live = col < k;
-  const int64_t iters = tn0 < tiles_n ? ceil_div(tiles_n - tn0, rows_in_flight) : 0;
-  auto tile_of = [&](int64_t it) {
-    return tn0 + (kQuant ? iters - 1 - it : it) * rows_in_flight;
-  };
-  if (lane == 0) {
-#pragma unroll
-    for (int st = 0; st < kR4Stages; ++st) core::mbar_init(&bars[st], 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+// The per-warp ring of one pass: which stage holds sequence position i, and
+// the parity each stage's barrier completes with next (bit st).  With two
+// stages, position i of a pass sits in stage (base + i) & 1; a pass that
+// walks the previous pass's tiles backwards starts with base = iters - 1 on
+// the two tiles that pass left resident.
+struct R4Ring {
+  uint8_t *ring, *rows;
+  uint64_t *bars;
+  uint32_t parity;
+};
+static_assert(kR4Stages == 2, "the resident-tile hand-over assumes two stages");
+
+template <typename TileOf>
+__device__ __forceinline__ void r4_prime(const R4Maps &tm, R4Ring &rg, int64_t iters,
+                                         TileOf tile_of, int64_t col0, int k, int lane) {
+  if (lane == 0)
     for (int d = 0; d < kR4Stages && d < iters; ++d)
-      r4_issue(tm, ring + d * kR4StageBytes, rows + d * kR4RowStride, &bars[d], tile_of(d),
-               col0, k);
-  }
+      r4_issue(tm, rg.ring + d * kR4StageBytes, rg.rows + d * kR4RowStride, &rg.bars[d],
+               tile_of(d), col0, k);
   __syncwarp();
-  const float *vc = vt + c * kVtPitch;
-  for (int64_t it = 0; it < iters; ++it) {
-    const int64_t tn = tile_of(it);
-    const int st = int(it % kR4Stages);
-    const bool arrived =
-        core::mbar_wait(&bars[st], unsigned(it / kR4Stages) & 1u, &never);
-    if (!__all_sync(0xFFFFFFFFu, arrived)) {
-      if (lane == 0) {
-        raise_status(status, kDevTimeout);
-        for (int64_t j = it + 1; j < it + kR4Stages && j < iters; ++j)
-          core::mbar_wait(&bars[j % kR4Stages], unsigned(j / kR4Stages) & 1u, &never);
+}
+
+// One pass of a warp over its iters row tiles in the order tile_of(i).
+// `resident` tiles at the start of the sequence are already in the ring
+// (the previous pass waited for them).  Returns false if a ring wait gave up
+// (kDevTimeout is raised and the warp's other copies in flight are waited
+// for, bounded).
+template <bool kQuant, typename TileOf>
+__device__ __forceinline__ bool r4_pass(const R4Maps &tm, R4Ring &rg, int64_t iters,
+                                        int64_t base, int resident, TileOf tile_of,
+                                        int64_t col0, int k, int n, int64_t tiles_k,
+                                        int64_t tk, const float *vc, int lane, float g_enc,
+                                        const float *rcp_tab, bool ok, float &mx,
+                                        uint8_t *__restrict__ packed,
+                                        uint8_t *__restrict__ scales, volatile int *never,
+                                        unsigned *status) {
+  const int g = lane >> 2, c = lane & 3;
+  const int64_t col = col0 + 32 * c;
+  const bool live = col < k;
+  for (int64_t i = 0; i < iters; ++i) {
+    const int64_t tn = tile_of(i);
+    const int st = int((base + i) & 1);
+    if (i >= resident) {
+      const bool arrived = core::mbar_wait(&rg.bars[st], (rg.parity >> st) & 1u, never);
+      if (!__all_sync(0xFFFFFFFFu, arrived)) {
+        if (lane == 0) {
+          raise_status(status, kDevTimeout);
+          const int other = st ^ 1;
+          if (i + 1 < iters && i + 1 >= resident)
+            core::mbar_wait(&rg.bars[other], (rg.parity >> other) & 1u, never);
+        }
+        return false;
       }
-      break;
+      rg.parity ^= 1u << st;
     }
     uint4 w[2][4];
-    r4_read(ring + st * kR4StageBytes, g, c, w);
-    const R4Row rw[2] = {r4_row(rows + st * kR4RowStride, g),
-                         r4_row(rows + st * kR4RowStride, 8 + g)};
+    r4_read(rg.ring + st * kR4StageBytes, g, c, w);
+    const R4Row rw[2] = {r4_row(rg.rows + st * kR4RowStride, g),
+                         r4_row(rg.rows + st * kR4RowStride, 8 + g)};
     __syncwarp();
-    if (lane == 0 && it + kR4Stages < iters)
-      r4_issue(tm, ring + st * kR4StageBytes, rows + st * kR4RowStride, &bars[st],
-               tile_of(it + kR4Stages), col0, k);
+    if (lane == 0 && i + kR4Stages < iters)
+      r4_issue(tm, rg.ring + st * kR4StageBytes, rg.rows + st * kR4RowStride, &rg.bars[st],
+               tile_of(i + kR4Stages), col0, k);
     uint32_t sword = 0;
     if (live) {
       uint64_t nu[2][4];
@@ -647,7 +639,61 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     if (kQuant) reinterpret_cast<uint32_t *>(scales + (tn * tiles_k + tk) * 128)[lane] = sword;
   }
-  if (!kQuant) {
+  return true;
+}
+
+// The rank-4 passes.  kR4Amax: max |e| over the tensor into amax_bits[0] as
+// bf16 bits (like amax_kernel).  kR4Quant: the quantisation pass.  kR4Both:
+// both in one cooperative launch -- every CTA folds its maximum into
+// amax_bits[0], arrives on amax_bits[1] and waits (bounded) until all CTAs
+// have; the quantisation pass then walks each warp's tiles backwards,
+// starting on the two the amax pass left in its ring.  amax_bits[0..1] are
+// zero at the start of the call.
+constexpr int kR4Amax = 0, kR4Quant = 1, kR4Both = 2;
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 2)
+    recon_r4_kernel(const __grid_constant__ R4Maps tm, const uint16_t *__restrict__ V, int n,
+                    int k, uint8_t *__restrict__ packed,
+                    uint8_t *__restrict__ scales, float *__restrict__ global_scale,
+                    uint32_t *amax_bits, unsigned *status) {
+  extern __shared__ uint8_t r4_smem_raw[];
+  __shared__ float rcp_tab[128];
+  __shared__ int never;  // abort flag of the bounded waits; nothing sets it
+  __shared__ int grid_ok;
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(r4_smem_raw) + 1023) & ~uintptr_t(1023));
+  const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31, c = lane & 3;
+  R4Ring rg{smem + wi * kR4Stages * kR4StageBytes,
+            smem + kR4RowsOffset + wi * kR4Stages * kR4RowStride,
+            reinterpret_cast<uint64_t *>(smem + kR4BarsOffset) + wi * kR4Stages, 0u};
+  float *vt = reinterpret_cast<float *>(smem + kR4RingBytes) + wi * kVtFloats;
+  const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
+  const int64_t nw = int64_t(gridDim.x) * kR4Warps, w = int64_t(blockIdx.x) * kR4Warps + wi;
+  const int64_t tk = w % tiles_k, col0 = tk * kTileCols, tn0 = w / tiles_k;
+  const int64_t rows_in_flight = nw / tiles_k + (tk < nw % tiles_k ? 1 : 0);
+  const int64_t iters = tn0 < tiles_n ? ceil_div(tiles_n - tn0, rows_in_flight) : 0;
+  auto fwd = [&](int64_t i) { return tn0 + i * rows_in_flight; };
+  auto rev = [&](int64_t i) { return tn0 + (iters - 1 - i) * rows_in_flight; };
+  if (threadIdx.x == 0) never = 0;
+  if (lane == 0) {
+#pragma unroll
+    for (int st = 0; st < kR4Stages; ++st) core::mbar_init(&rg.bars[st], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (kMode == kR4Quant)
+    r4_prime(tm, rg, iters, rev, col0, k, lane);
+  else
+    r4_prime(tm, rg, iters, fwd, col0, k, lane);
+  stage_vt(V, col0, k, lane, vt);
+  __syncthreads();
+  const float *vc = vt + c * kVtPitch;
+  bool ring_ok = true;
+
+  if (kMode != kR4Quant) {
+    float mx = 0.0f;
+    ring_ok = r4_pass<false>(tm, rg, iters, 0, 0, fwd, col0, k, n, tiles_k, tk, vc, lane, 1.0f,
+                             rcp_tab, true, mx, nullptr, nullptr, &never, status);
     // bf16 bits of the largest |e|: a NaN stays a NaN pattern and an
     // infinity the infinity pattern, both at or above 0x7F80
     const uint32_t m = __float_as_uint(mx);
@@ -656,6 +702,48 @@ __global__ void __launch_bounds__(kThreads, 2)
     mb = block_max_u32(mb);
     if (threadIdx.x == 0) atomicMax(amax_bits, mb);
   }
+  if (kMode == kR4Amax) return;
+
+  if (kMode == kR4Both) {
+    // grid barrier: release this CTA's maximum, count it in, wait for all
+    if (threadIdx.x == 0) {
+      int ok_all = 1;
+      __threadfence();
+      atomicAdd(amax_bits + 1, 1u);
+      unsigned seen = 0;
+      for (unsigned it = 0;; ++it) {
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(seen) : "l"(amax_bits + 1)
+                     : "memory");
+        if (seen >= gridDim.x) break;
+        if (it >= core::kSpinLimit) {
+          raise_status(status, kDevTimeout);
+          ok_all = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+      grid_ok = ok_all;
+    }
+    __syncthreads();
+    if (!grid_ok) return;
+  }
+
+  float g_enc = 1.0f, g_dec = 1.0f;
+  uint32_t ab;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(ab) : "l"(amax_bits) : "memory");
+  const bool ok = global_scales(ab, g_enc, g_dec);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *global_scale = ok ? g_dec : __int_as_float(0x7FC00000);
+    if (!ok) raise_status(status, kDevRange);
+  }
+  fill_rcp_table(g_enc, rcp_tab);
+  __syncthreads();
+  if (!ring_ok) return;
+  float unused = 0.0f;
+  const int resident = kMode == kR4Both ? int(iters < kR4Stages ? iters : kR4Stages) : 0;
+  const int64_t base = kMode == kR4Both ? iters - 1 : 0;
+  r4_pass<true>(tm, rg, iters, base, resident, rev, col0, k, n, tiles_k, tk, vc, lane, g_enc,
+                rcp_tab, ok, unused, packed, scales, &never, status);
 }
 
 // Activations for the block-scaled MMA path (reading R9: each token row
@@ -754,19 +842,36 @@ static void quantize_pass(const uint16_t *W, const float *s, const uint16_t *U,
                                                      dev.status);
 }
 
-// Rank 4: CTA j works tile column j % tiles_k with its eight warps on row
-// tiles 8 (j / tiles_k) + w + 8 Q i (Q CTAs per tile column), at most two
-// CTAs per SM in one wave.
-template <bool kQuant>
+// Rank 4: two CTAs per SM (fewer for a small tensor), so that every SM
+// carries the same number of warps; every tile column needs a warp, and
+// when that takes more CTAs than fit on the GPU at once the two passes run
+// as two launches, else as one cooperative launch (kR4Both).
+template <int kMode>
 static cudaError_t r4_smem_attr(int device) {
   static bool done[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
   const cudaError_t e = cudaFuncSetAttribute(
-      recon_r4_kernel<kQuant>, cudaFuncAttributeMaxDynamicSharedMemorySize, kR4SmemBytes);
+      recon_r4_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kR4SmemBytes);
   if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
   return e;
+}
+
+// CTAs of the cooperative form that can be resident at once (0 if unknown).
+static int64_t r4_both_capacity(const DeviceInfo &dev) {
+  static int per_sm[64] = {};
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev.ordinal < 0 || dev.ordinal >= 64) return 0;
+  if (per_sm[dev.ordinal] == 0) {
+    int nb = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, recon_r4_kernel<kR4Both>, kThreads,
+                                                      kR4SmemBytes) != cudaSuccess)
+      nb = -1;
+    per_sm[dev.ordinal] = nb > 0 ? nb : -1;
+  }
+  return per_sm[dev.ordinal] > 0 ? int64_t(per_sm[dev.ordinal]) * dev.sms : 0;
 }
 
 static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uint16_t *U,
@@ -778,19 +883,28 @@ static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uin
       !core::encode_bytes_1d(U, uint64_t(n) * 8, kTileRows * 8, &tm.u) ||
       !core::encode_bytes_1d(s, uint64_t(n) * 4, kTileRows * 4, &tm.s))
     return cudaErrorInvalidValue;
-  cudaError_t e = r4_smem_attr<false>(dev.ordinal);
-  if (e == cudaSuccess) e = r4_smem_attr<true>(dev.ordinal);
+  cudaError_t e = r4_smem_attr<kR4Amax>(dev.ordinal);
+  if (e == cudaSuccess) e = r4_smem_attr<kR4Quant>(dev.ordinal);
+  if (e == cudaSuccess) e = r4_smem_attr<kR4Both>(dev.ordinal);
   if (e != cudaSuccess) return e;
   const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
-  int64_t Q = int64_t(dev.sms) * 2 / tiles_k;
-  if (Q > ceil_div(tiles_n, kR4Warps)) Q = ceil_div(tiles_n, kR4Warps);
-  if (Q < 1) Q = 1;
-  const int g = int(tiles_k * Q);
-  recon_r4_kernel<false><<<g, kThreads, kR4SmemBytes, st>>>(tm, V, n, k, int(Q), nullptr,
-                                                           nullptr, nullptr, amax, dev.status);
-  recon_r4_kernel<true><<<g, kThreads, kR4SmemBytes, st>>>(tm, V, n, k, int(Q), out.packed,
-                                                          out.scales, out.global_scale, amax,
-                                                          dev.status);
+  int64_t G = ceil_div(tiles_k * tiles_n, kR4Warps);
+  if (G > int64_t(dev.sms) * 2) G = int64_t(dev.sms) * 2;
+  if (G < ceil_div(tiles_k, kR4Warps)) G = ceil_div(tiles_k, kR4Warps);
+  const int g = int(G);
+  uint8_t *packed = out.packed, *scales = out.scales;
+  float *gs = out.global_scale;
+  unsigned *status = dev.status;
+  if (g <= r4_both_capacity(dev)) {
+    void *args[] = {&tm, const_cast<uint16_t **>(&V), &n, &k, &packed, &scales, &gs, &amax,
+                    &status};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(recon_r4_kernel<kR4Both>),
+                                       dim3(g), dim3(kThreads), args, kR4SmemBytes, st);
+  }
+  recon_r4_kernel<kR4Amax><<<g, kThreads, kR4SmemBytes, st>>>(tm, V, n, k, nullptr, nullptr,
+                                                             nullptr, amax, status);
+  recon_r4_kernel<kR4Quant><<<g, kThreads, kR4SmemBytes, st>>>(tm, V, n, k, packed, scales, gs,
+                                                              amax, status);
   return cudaGetLastError();
 }
 
@@ -798,8 +912,8 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
                             const uint16_t *V, int r, bool fused, int n, int k,
                             const aq_nvfp4_weight &out, void *ws, const DeviceInfo &dev,
                             cudaStream_t st) {
-  uint32_t *amax = static_cast<uint32_t *>(ws);
-  cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(uint32_t), st);
+  uint32_t *amax = static_cast<uint32_t *>(ws);  // [0] amax bits, [1] grid arrivals
+  cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
   if (!fused)
     quantize_pass<0, false>(W, s, U, V, 0, n, k, out, amax, dev, st);
