@@ -232,7 +232,7 @@ class Stack:
         import torch
         from nvfp4_block_scaled_aq_gb300 import aq, inputs
         self.shapes, self.layers, self.m = shapes, layers, m
-        qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+        qws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
         self.weights = []
         for layer in range(layers):
             for p, (n, k) in enumerate(shapes):
@@ -359,7 +359,7 @@ def epilogue_leg(stream, dist, a, device):
     for c in range(2):
         W = inputs.weight(n, k, seed=inputs.seed_of(9100 + c), device=device)
         w = aq.Nvfp4Weight.empty(n, k, device=device)
-        aq.quantize(W, w, torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8,
+        aq.quantize(W, w, torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8,
                                       device=device))
         ws_w.append(w)
         del W
@@ -414,7 +414,7 @@ def small_gemv_timing(n, k, copies, pdl, stream, dist, a, device):
     between the calls; event-timed on the launching stream."""
     import torch
     from nvfp4_block_scaled_aq_gb300 import aq, inputs
-    qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+    qws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
     ws_w = []
     for c in range(copies):
         W = inputs.weight(n, k, seed=inputs.seed_of(9700 + c), device=device)
@@ -503,7 +503,7 @@ def run_profile_case(a, dist):
     torch.cuda.set_device(dist.local)
     device = torch.device("cuda", dist.local)
     n, k = inputs.LAYER_31B[a.profile_proj]
-    qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+    qws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
     if a.profile_case == "load":
         th = inputs.theta(n, k, 4, seed=inputs.seed_of(9800), device=device)
         w = aq.Nvfp4Weight.empty(n, k, device=device)
@@ -822,7 +822,7 @@ def run_load_time(a, dist):
     stream = torch.cuda.Stream(device)
     r = 4
     shapes = [("1b_gate_up", 13824, 1152), ("1b_down", 1152, 6912), ("31b_gate_up", 43008, 5376)]
-    qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+    qws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
     rows = []
     for name, n, k in shapes:
         copies = max(1, -(-(256 << 20) // (2 * n * k)))
@@ -884,7 +884,7 @@ def run_sweep(a, dist):
     torch.cuda.set_device(dist.local)
     device = torch.device("cuda", dist.local)
     stream = torch.cuda.Stream(device)
-    qws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
+    qws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=device)
     results = []
     ms = tuple(int(v) for v in a.sweep_m.split(",")) if a.sweep_m else SWEEP_M
     projs = {"both": (2, 3), "gate_up": (2,), "down": (3,)}[a.sweep_proj]

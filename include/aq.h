@@ -117,8 +117,13 @@ AQ_API aq_status aq_reconstruct(const uint16_t *W0, const float *s, const uint16
                          uint16_t *W_eff, aq_stream_t stream);
 
 /* Workspace of aq_quantize_nvfp4 and aq_reconstruct_quantize_nvfp4: at
- * least this many bytes, 256-byte aligned, device memory.  Its contents
- * need no initialisation. */
+ * least this many bytes, 256-byte aligned, device memory.  It must be
+ * ZERO-FILLED once after allocation; every call leaves it zeroed (its
+ * quantisation pass clears the amax and the grid-barrier words once all of
+ * its CTAs have read them), so one workspace serves any sequence of calls on
+ * one stream.  Calls that may run concurrently need separate workspaces.  A
+ * call after which aq_poll_device_status reports AQ_ERR_TIMEOUT may leave
+ * it dirty: zero it again before the next call. */
 AQ_API size_t aq_quantize_workspace_bytes(void);
 
 /* Round-to-nearest NVFP4 quantisation of a bf16 weight W [n, k] into *out

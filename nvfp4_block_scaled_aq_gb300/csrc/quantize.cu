@@ -172,6 +172,22 @@ __device__ __forceinline__ bool global_scales(uint32_t amax_bits, float &g_enc,
   return !isinf(g_enc);
 }
 
+// Called by every thread of a CTA after a __syncthreads that follows all of
+// its threads' reads of the amax word: the CTA counts itself out on
+// ws[2], and the last CTA of the grid clears ws[0..2] (amax, grid
+// arrivals, departures), so the call leaves the workspace zeroed.
+__device__ __forceinline__ void depart_and_clear(uint32_t *ws) {
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(ws + 2, 1u) == gridDim.x - 1) {
+      ws[0] = 0;
+      ws[1] = 0;
+      ws[2] = 0;
+      __threadfence();
+    }
+  }
+}
+
 // Two fp32 -> bf16x2 (nearest even), `hi` in the upper half.
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float hi, float lo) {
   uint32_t r;
@@ -275,7 +291,7 @@ __global__ void __launch_bounds__(kThreads)
                     const uint16_t *__restrict__ U, const uint16_t *__restrict__ V,
                     int n, int k, int r, uint8_t *__restrict__ packed,
                     uint8_t *__restrict__ scales, float *__restrict__ global_scale,
-                    const uint32_t *__restrict__ amax_bits, unsigned *status) {
+                    uint32_t *amax_bits, unsigned *status) {
   float g_enc = 1.0f, g_dec = 1.0f;
   const bool ok = global_scales(*amax_bits, g_enc, g_dec);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -285,6 +301,7 @@ __global__ void __launch_bounds__(kThreads)
   __shared__ float rcp_tab[128];
   fill_rcp_table(g_enc, rcp_tab);
   __syncthreads();
+  depart_and_clear(amax_bits);
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, c = lane & 3;
   const int64_t tiles_k = ceil_div(k, kTileCols);
@@ -647,8 +664,9 @@ __device__ __forceinline__ bool r4_pass(const R4Maps &tm, R4Ring &rg, int64_t it
 // both in one cooperative launch -- every CTA folds its maximum into
 // amax_bits[0], arrives on amax_bits[1] and waits (bounded) until all CTAs
 // have; the quantisation pass then walks each warp's tiles backwards,
-// starting on the two the amax pass left in its ring.  amax_bits[0..1] are
-// zero at the start of the call.
+// starting on the two the amax pass left in its ring.  amax_bits[0..2] are
+// zero at the start of the call, and the quantisation pass leaves them so
+// (depart_and_clear).
 constexpr int kR4Amax = 0, kR4Quant = 1, kR4Both = 2;
 
 template <int kMode>
@@ -738,6 +756,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   }
   fill_rcp_table(g_enc, rcp_tab);
   __syncthreads();
+  depart_and_clear(amax_bits);
   if (!ring_ok) return;
   float unused = 0.0f;
   const int resident = kMode == kR4Both ? int(iters < kR4Stages ? iters : kR4Stages) : 0;
@@ -912,9 +931,9 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
                             const uint16_t *V, int r, bool fused, int n, int k,
                             const aq_nvfp4_weight &out, void *ws, const DeviceInfo &dev,
                             cudaStream_t st) {
-  uint32_t *amax = static_cast<uint32_t *>(ws);  // [0] amax bits, [1] grid arrivals
-  cudaError_t e = cudaMemsetAsync(amax, 0, 2 * sizeof(uint32_t), st);
-  if (e != cudaSuccess) return e;
+  // [0] amax bits, [1] grid arrivals, [2] departures: zero on entry, and
+  // zero again when the quantisation pass is done
+  uint32_t *amax = static_cast<uint32_t *>(ws);
   if (!fused)
     quantize_pass<0, false>(W, s, U, V, 0, n, k, out, amax, dev, st);
   else if (r == 4 && ((reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(U) |

@@ -24,7 +24,7 @@ def require_gpu():
 def quantize_gpu(W):
     n, k = W.shape
     w = aq.Nvfp4Weight.empty(n, k, device=W.device)
-    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=W.device)
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=W.device)
     aq.quantize(W, w, ws)
     return w
 

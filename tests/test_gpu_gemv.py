@@ -165,7 +165,7 @@ def test_passthrough_gemv_equals_plain_gemv_bit_exact():
     n, k = 13824, 1152
     th = inputs.theta(n, k, 4, seed=17, device=DEV, passthrough=True)
     w_theta = aq.Nvfp4Weight.empty(n, k, device=DEV)
-    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
     aq.reconstruct_quantize(th.W0, th.s, th.U, th.V, w_theta, ws)
     w_plain = quantize_gpu(th.W0)
     x = inputs.tokens(1, k, seed=18, device=DEV)

@@ -175,7 +175,7 @@ def test_fused_reconstruct_quantize_bit_exact(n, k, r, passthrough):
     quantise; at passthrough it equals quantising W0 itself."""
     th = inputs.theta(n, k, r, seed=11 + n, device=DEV, passthrough=passthrough)
     w = aq.Nvfp4Weight.empty(n, k, device=DEV)
-    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
     aq.reconstruct_quantize(th.W0, th.s, th.U, th.V, w, ws)
     W_eff = oracle.reconstruct(bits(th.W0), th.s.cpu().numpy(), bits(th.U), bits(th.V))
     if passthrough:
@@ -201,7 +201,7 @@ def test_rank4_v_alignment_paths_bit_exact(offset):
     aq.reconstruct(th.W0, th.s, th.U, V, W_eff)
     assert np.array_equal(bits(W_eff), ref)
     w = aq.Nvfp4Weight.empty(n, k, device=DEV)
-    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
     aq.reconstruct_quantize(th.W0, th.s, th.U, V, w, ws)
     assert_quantized_equal(w, ref)
     assert aq.poll_device_status() == aq.OK
@@ -227,7 +227,7 @@ def test_rank4_u_s_alignment_fallback_bit_exact(which):
         assert s.data_ptr() % 16 == 4
     ref = oracle.reconstruct(bits(th.W0), th.s.cpu().numpy(), bits(th.U), bits(th.V))
     w = aq.Nvfp4Weight.empty(n, k, device=DEV)
-    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
     aq.reconstruct_quantize(th.W0, s, U, th.V, w, ws)
     assert_quantized_equal(w, ref)
     assert aq.poll_device_status() == aq.OK
@@ -236,7 +236,7 @@ def test_rank4_u_s_alignment_fallback_bit_exact(which):
 def _fused_r4(W0b, s, Ub, Vb):
     n, k = W0b.shape
     w = aq.Nvfp4Weight.empty(n, k, device=DEV)
-    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
     aq.reconstruct_quantize(to_dev(W0b), torch.as_tensor(s, device=DEV), to_dev(Ub),
                             to_dev(Vb), w, ws)
     return w
@@ -253,7 +253,7 @@ def test_rank4_packed_path_ragged_shapes_bit_exact(n, k):
     th = inputs.theta(n, k, 4, seed=n * 7 + k, device=DEV)
     assert th.V.data_ptr() % 16 == 0
     w = aq.Nvfp4Weight.empty(n, k, device=DEV)
-    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
     aq.reconstruct_quantize(th.W0, th.s, th.U, th.V, w, ws)
     ref = oracle.reconstruct(bits(th.W0), th.s.cpu().numpy(), bits(th.U), bits(th.V))
     assert_quantized_equal(w, ref)

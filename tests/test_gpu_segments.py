@@ -23,7 +23,7 @@ def _gpu():
 def quantize_segments_gpu(W, seg_end):
     n, k = W.shape
     w = aq.Nvfp4Weight.empty(n, k, device=DEV, nscales=len(seg_end))
-    ws = torch.empty(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
     aq.quantize_segments(W, seg_end, w, ws)
     torch.cuda.synchronize()
     return w
