@@ -46,9 +46,9 @@ NCU_TRAFFIC = {
     # weight of the layer can still sit in L2 from an earlier step), m = 1,
     # one-token kernel form, captured without cache flushing so the L2
     # prefetch of the next projection counts where it is issued: reads
-    # 19,208,704 + 14,810,368 + 144,470,528 + 67,886,080, writes 183,296 +
-    # 83,456 + 466,688 + 254,464 (the committed ncu summary of that capture)
-    ("gemma4-31b-shaped decode-step weight stream", 1, "4b88f539555eb6e9b267da702207c4f762e9f0f0"): 247363584,
+    # 19,524,096 + 15,062,016 + 143,823,616 + 67,985,664, writes 223,744 +
+    # 86,016 + 469,504 + 228,352 (the committed ncu summary of that capture)
+    ("gemma4-31b-shaped decode-step weight stream", 1, "a32985606f8cc6865ecca4601cbd5245b8dbc79f"): 247403008,
 }
 
 

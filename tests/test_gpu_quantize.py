@@ -328,3 +328,27 @@ def test_rank4_non_finite_w_eff_sets_status(case):
     assert aq.poll_device_status() == aq.ERR_RANGE
     gp, gs, gd = weight_bytes(w)
     assert not gp.any() and not gs.any() and np.isnan(gd)
+
+
+def test_one_workspace_serves_every_path_and_is_left_zeroed():
+    """A quantise workspace zero-filled once serves a sequence of calls on
+    every path -- plain quantise, the cooperative rank-4 form, its two-launch
+    form, the generic-rank form -- and each call leaves its words zero."""
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    cases = [("plain", 100, 2048, 0), ("r4", 300, 1152, 4), ("r4", 16, 320000, 4),
+             ("generic", 37, 96, 3), ("r4", 45, 160, 4)]
+    for i, (form, n, k, r) in enumerate(cases):
+        th = inputs.theta(n, k, max(r, 1), seed=200 + i, device=DEV)
+        w = aq.Nvfp4Weight.empty(n, k, device=DEV)
+        if form == "plain":
+            aq.quantize(th.W0, w, ws)
+            ref = bits(th.W0)
+        else:
+            U = th.U[:, :r].contiguous()
+            V = th.V[:, :r].contiguous()
+            aq.reconstruct_quantize(th.W0, th.s, U, V, w, ws)
+            ref = oracle.reconstruct(bits(th.W0), th.s.cpu().numpy(), bits(U), bits(V))
+        torch.cuda.synchronize()
+        assert not ws.any().item(), (form, n, k)
+        assert_quantized_equal(w, ref)
+        assert aq.poll_device_status() == aq.OK
