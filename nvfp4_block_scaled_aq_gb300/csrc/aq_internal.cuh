@@ -194,10 +194,12 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
                             const aq_nvfp4_weight &out, void *ws, const DeviceInfo &dev,
                             cudaStream_t st);
 // Per-row NVFP4 quantisation of activations (quantize.cu); scales row-major
-// with a pitch of scale_pitch bytes.
+// with a pitch of scale_pitch bytes.  pdl: launched as a programmatic
+// dependent of the previous kernel on the stream (it waits for it before
+// reading x); either way the kernel lets its own dependents start early.
 cudaError_t launch_act_quant(const uint16_t *x, int m, int k, uint8_t *packed, uint8_t *scales,
                              int scale_pitch, float *g_dec, const DeviceInfo &dev,
-                             cudaStream_t st);
+                             cudaStream_t st, bool pdl = false);
 cudaError_t launch_scales_to_canonical(const aq_nvfp4_weight &w, uint8_t *canon,
                                        cudaStream_t st);
 cudaError_t launch_interleave_gate_up(const uint16_t *w, int f, int k, uint16_t *out,

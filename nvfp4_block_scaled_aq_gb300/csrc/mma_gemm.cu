@@ -134,10 +134,30 @@ __global__ void __launch_bounds__(kMmaThreads, 2)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      // the activations may come from the previous kernel in the stream
+      // The weight nibbles and scales of the first ring stages do not depend
+      // on the previous kernel (the activation quantisation): they are
+      // issued before the dependent-launch wait, the activation boxes of
+      // those stages after it.
+      const int64_t pre = u_end - u_begin < S ? u_end - u_begin : S;
+      for (int64_t i = 0; i < pre; ++i) {
+        const int64_t u = u_begin + i, rb = u / units;
+        const int uk = int(u - rb * units);
+        uint8_t *stage = ring + i * SB;
+        mbar_expect_tx(&ct.full[i], tx_bytes(N));
+        tma_load_2d(stage, &tm_w, uk * kUnitCols, int(rb * kRB), &ct.full[i]);
+        tma_load_2d(stage + kPackedStage, &tm_s, uk * kKT * 128, int(rb * kRG), &ct.full[i]);
+      }
       pdl_wait();
       RingPos pos;
-      for (int64_t u = u_begin; u < u_end; ++u, pos.advance(S)) {
+      for (int64_t i = 0; i < pre; ++i, pos.advance(S)) {
+        const int64_t u = u_begin + i, rb = u / units;
+        const int uk = int(u - rb * units);
+        uint8_t *stage = ring + i * SB;
+        (void)rb;
+        tma_load_2d(stage + st_b(N), &tm_x, uk * kUnitCols, 0, &ct.full[i]);
+        tma_load_2d(stage + st_sfb(N), &tm_xs, uk * 16, 0, &ct.full[i]);
+      }
+      for (int64_t u = u_begin + pre; u < u_end; ++u, pos.advance(S)) {
         const int st = pos.st;
         if (pos.wrapped && !wait_or_abort(&ct.empty[st], pos.phase ^ 1u, aborted, r.status)) break;
         if (*aborted) break;
@@ -415,7 +435,15 @@ cudaError_t launch_mma(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint1
   uint8_t *xq = wsb + lay.xq_off;
   uint8_t *xs = wsb + lay.xs_off;
   float *xg = reinterpret_cast<float *>(wsb + lay.xg_off);
-  cudaError_t e = launch_act_quant(x, m, w.k, xq, xs, lay.scale_pitch, xg, dev, st);
+  // Both kernels are launched as programmatic dependents.  The activation
+  // quantisation waits for whatever precedes it before it reads x or writes
+  // the workspace, so that is safe after any kernel (one that never lets
+  // dependents start early simply finishes first), and it lets the MMA
+  // kernel start streaming weights while the previous kernel drains and x
+  // is quantised; the MMA kernel waits for the quantisation before it reads
+  // the quantised activations or touches the workspace.
+  (void)pdl;
+  cudaError_t e = launch_act_quant(x, m, w.k, xq, xs, lay.scale_pitch, xg, dev, st, true);
   if (e != cudaSuccess) return e;
 
   const GemvPlan plan = plan_gemv(w.n, w.k, dev, 8);
@@ -459,7 +487,7 @@ cudaError_t launch_mma(const aq_nvfp4_weight &w, const uint16_t *x, int m, uint1
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, mma_gemm_kernel, tm_w, tm_s, tm_x, tm_xs, p, r, a);
 }
 

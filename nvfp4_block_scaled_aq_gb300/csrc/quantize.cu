@@ -775,6 +775,11 @@ __global__ void __launch_bounds__(kThreads)
                      uint8_t *__restrict__ scales, int scale_pitch, float *__restrict__ g_dec,
                      unsigned *status) {
   __shared__ uint32_t amax_s;
+  // Launched with programmatic dependent launch: the MMA kernel that
+  // follows may start now (it waits for this grid before it reads the
+  // quantised activations); x and the outputs wait for the previous kernel.
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t row = blockIdx.x;
   const uint16_t *xr = x + row * k;
   uint32_t m2 = 0;
@@ -950,9 +955,18 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
 
 cudaError_t launch_act_quant(const uint16_t *x, int m, int k, uint8_t *packed, uint8_t *scales,
                              int scale_pitch, float *g_dec, const DeviceInfo &dev,
-                             cudaStream_t st) {
-  act_quant_kernel<<<m, kThreads, 0, st>>>(x, k, packed, scales, scale_pitch, g_dec, dev.status);
-  return cudaGetLastError();
+                             cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(m);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, act_quant_kernel, x, k, packed, scales, scale_pitch, g_dec,
+                            dev.status);
 }
 
 // out row 16 j + i = gate row 8 j + i, out row 16 j + 8 + i = up row 8 j + i

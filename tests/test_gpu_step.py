@@ -271,3 +271,33 @@ def test_31b_step_pdl_graph_sampled_parity():
     assert aq.poll_device_status() == aq.OK
     for i, (a, b) in enumerate(zip(ys, chain)):
         assert torch.equal(a, b), "persistent step differs from the chain at projection %d" % i
+
+
+@pytest.mark.parametrize("flag", ["regdecode", "mma"])
+@pytest.mark.parametrize("m", [1, 4])
+def test_step_chained_projections_wait_for_their_inputs(flag, m):
+    """Each projection's input is the previous projection's output (square
+    weights, x of projection p + 1 aliasing y of projection p), launched as
+    one step with programmatic dependent launch: every kernel that reads x
+    (the GEMV's activation staging, the MMA path's activation quantisation)
+    must wait for the kernel that wrote it.  The result equals the same
+    chain run call by call."""
+    n = 1152
+    layers = [(n, n)] * 6
+    ws = [quantize_gpu(inputs.weight(n, n, seed=inputs.seed_of(31, 0, p), device=DEV))
+          for p in range(len(layers))]
+    x0 = inputs.tokens(m, n, seed=32, device=DEV)
+    ys = [torch.empty((m, n), dtype=torch.bfloat16, device=DEV) for _ in layers]
+    xs = [x0] + ys[:-1]
+    fl = {"regdecode": aq.STEP_REGDECODE, "mma": aq.STEP_MMA}[flag]
+    path = {"regdecode": aq.PATH_GEMV_REGDECODE, "mma": aq.PATH_MMA}[flag]
+    wsp = step_workspace(layers, m)
+    aq.decode_step(aq.StepArgs(ws, xs, ys), wsp, flags=aq.STEP_PDL | fl)
+    torch.cuda.synchronize()
+    x = x0
+    for i, w in enumerate(ws):
+        y = gemv_gpu(w, x, path=path)
+        torch.cuda.synchronize()
+        assert torch.equal(ys[i], y), "projection %d" % i
+        x = y
+    assert aq.poll_device_status() == aq.OK
