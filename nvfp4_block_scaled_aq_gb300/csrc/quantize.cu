@@ -699,6 +699,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int st = 0; st < kR4Stages; ++st) core::mbar_init(&rg.bars[st], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  // Launched as a programmatic dependent: the next call may start now, and
+  // this one reads its inputs and the workspace only once the previous
+  // kernel on the stream has finished.
+  pdl_launch_dependents();
+  pdl_wait();
   if (kMode == kR4Quant)
     r4_prime(tm, rg, iters, rev, col0, k, lane);
   else
@@ -919,17 +924,29 @@ static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uin
   uint8_t *packed = out.packed, *scales = out.scales;
   float *gs = out.global_scale;
   unsigned *status = dev.status;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kR4SmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
   if (g <= r4_both_capacity(dev)) {
-    void *args[] = {&tm, const_cast<uint16_t **>(&V), &n, &k, &packed, &scales, &gs, &amax,
-                    &status};
-    return cudaLaunchCooperativeKernel(reinterpret_cast<void *>(recon_r4_kernel<kR4Both>),
-                                       dim3(g), dim3(kThreads), args, kR4SmemBytes, st);
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Both>, tm, V, n, k, packed, scales, gs,
+                              amax, status);
   }
-  recon_r4_kernel<kR4Amax><<<g, kThreads, kR4SmemBytes, st>>>(tm, V, n, k, nullptr, nullptr,
-                                                             nullptr, amax, status);
-  recon_r4_kernel<kR4Quant><<<g, kThreads, kR4SmemBytes, st>>>(tm, V, n, k, packed, scales, gs,
-                                                              amax, status);
-  return cudaGetLastError();
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Amax>, tm, V, n, k,
+                         static_cast<uint8_t *>(nullptr), static_cast<uint8_t *>(nullptr),
+                         static_cast<float *>(nullptr), amax, status);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Quant>, tm, V, n, k, packed, scales, gs,
+                            amax, status);
 }
 
 cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U,
