@@ -359,14 +359,13 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------- rank 4, packed fp32
-// The fused form for the configured rank (4) with V 16-byte aligned.  Warp w
-// of W works tile column w % tiles_k, whose W_c warps (W / tiles_k, one more
-// for the first W % tiles_k columns) take its row tiles in turn; the eight
-// warps of a CTA hold neighbouring tile columns, so a CTA reads 16-row bands
-// of up to 2 KB per row.  Lane
-// 4g + c owns rows g and g + 8 of each tile and columns [32c, 32c + 32): two
-// 16-element blocks per row, whose four E4M3 scales form the lane's word of
-// the scale layout.
+// The fused form for the configured rank (4) with V, U and s 16-byte
+// aligned.  Warp w of W works tile column w % tiles_k, whose W_c warps
+// (W / tiles_k, one more for the first W % tiles_k columns) take its row
+// tiles in turn; the eight warps of a CTA hold neighbouring tile columns, so
+// a CTA reads 16-row bands of up to 2 KB per row.  Lane 4g + c owns rows g
+// and g + 8 of each tile and columns [32c, 32c + 32): two 16-element blocks
+// per row, whose four E4M3 scales form the lane's word of the scale layout.
 //
 // The warp's 128 columns of V sit in shared memory as fp32, rank-major
 // (vt[t][c][j] = V[col0 + 32c + j][t]), so one 16-byte shared load gives
@@ -430,7 +429,7 @@ struct R4Row {
   uint32_t u01, u23;
 };
 
-// The weights reach shared memory through a three-stage ring per warp: a
+// The weights reach shared memory through a two-stage ring per warp: a
 // stage holds one row tile of the warp's tile column as two TMA boxes of 16
 // rows x 64 columns (128 bytes per row, 128-byte swizzle: 16-byte chunk j of
 // row r sits at chunk j ^ (r & 7)); rows past n and columns past k read as
