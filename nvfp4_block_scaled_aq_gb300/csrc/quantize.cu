@@ -501,54 +501,83 @@ __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
+// What r4_block does with one 16-column block of both rows:
+//   kFormAmax      rebuild (packed pairs), fold |e| into mx;
+//   kFormAmaxKeep  rebuild exactly (the quantisation pass's arithmetic), fold
+//                  |e| into mx, and write the bf16 W_eff pairs back over the
+//                  lane's W0 bytes in the stage;
+//   kFormQuant     rebuild exactly and quantise;
+//   kFormQuantEff  quantise the stage's bytes, which already hold W_eff.
+constexpr int kFormAmax = 0, kFormAmaxKeep = 1, kFormQuant = 2, kFormQuantEff = 3;
+
 // One 16-column block (columns 16b .. 16b + 15 of the lane's chunk) of both
-// rows.  nu[h][t] = (u_t, u_t) of row h (see r4_pairs).  The amax pass folds |e| into mx
-// (NaN-propagating maximum); the quantisation pass writes the block's two
-// packed words per row into out[h][2b], out[h][2b + 1] and returns the four
-// scale codes' contribution to the lane's scale word.
-template <bool kQuant>
+// rows.  nu[h][t] = (u_t, u_t) of row h (see r4_pairs).  mx takes the
+// NaN-propagating maximum of |e|; the quantising forms write the block's
+// two packed words per row into out[h][2b], out[h][2b + 1] and return the
+// four scale codes' contribution to the lane's scale word.  stage, g, c
+// locate the lane's bytes for kFormAmaxKeep's write-back.
+template <int kForm>
 __device__ __forceinline__ uint32_t r4_block(const uint4 (&w)[2][4], const R4Row (&rw)[2],
                                              const uint64_t (&nu)[2][4],
                                              const float *__restrict__ vc, int b, float g_enc,
                                              const float *__restrict__ rcp_tab, bool ok,
-                                             float &mx, uint32_t (&out)[2][4]) {
+                                             float &mx, uint32_t (&out)[2][4], uint8_t *stage,
+                                             int g, int c) {
+  constexpr bool kQuant = kForm == kFormQuant || kForm == kFormQuantEff;
   uint32_t bw[2][8];
-  // Half a block (8 columns, 4 pairs) of both rows at a time, rank-outer:
-  // eight independent fma chains per rank step.
+  if constexpr (kForm == kFormQuantEff) {
 #pragma unroll
-  for (int hb = 0; hb < 2; ++hb) {
-    uint64_t m[2][4] = {{0ull, 0ull, 0ull, 0ull}, {0ull, 0ull, 0ull, 0ull}};  // (+0, +0)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float *vr = vc + t * 4 * kVtPitch + 16 * b + 8 * hb;
-      const ulonglong2 va = *reinterpret_cast<const ulonglong2 *>(vr);
-      const ulonglong2 vb = *reinterpret_cast<const ulonglong2 *>(vr + 4);
+      for (int pi = 0; pi < 8; ++pi) bw[h][pi] = word_of(w[h][2 * b + (pi >> 2)], pi & 3);
+  } else {
+    // Half a block (8 columns, 4 pairs) of both rows at a time, rank-outer:
+    // eight independent fma chains per rank step.
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      uint64_t m[2][4] = {{0ull, 0ull, 0ull, 0ull}, {0ull, 0ull, 0ull, 0ull}};  // (+0, +0)
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float *vr = vc + t * 4 * kVtPitch + 16 * b + 8 * hb;
+        const ulonglong2 va = *reinterpret_cast<const ulonglong2 *>(vr);
+        const ulonglong2 vb = *reinterpret_cast<const ulonglong2 *>(vr + 4);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          m[h][0] = fma2(nu[h][t], va.x, m[h][0]);
+          m[h][1] = fma2(nu[h][t], va.y, m[h][1]);
+          m[h][2] = fma2(nu[h][t], vb.x, m[h][2]);
+          m[h][3] = fma2(nu[h][t], vb.y, m[h][3]);
+        }
+      }
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        m[h][0] = fma2(nu[h][t], va.x, m[h][0]);
-        m[h][1] = fma2(nu[h][t], va.y, m[h][1]);
-        m[h][2] = fma2(nu[h][t], vb.x, m[h][2]);
-        m[h][3] = fma2(nu[h][t], vb.y, m[h][3]);
-      }
-    }
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-#pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const int pi = 4 * hb + p;  // column pair within the block
-        const uint32_t wd = word_of(w[h][2 * b + hb], p);
-        if (kQuant) {
-          float mlo, mhi;
-          unpack2(m[h][p], mlo, mhi);
-          const float elo = __fmaf_rn(rw[h].s, bf16_lo(wd), -mlo);
-          const float ehi = __fmaf_rn(rw[h].s, bf16_hi(wd), -mhi);
-          bw[h][pi] = f32x2_to_bf16x2(ehi, elo);
-        } else {
-          const uint64_t e = fma2(pack2(-rw[h].s, -rw[h].s), bf16x2_to_f32x2(wd), m[h][p]);
-          float elo, ehi;
-          unpack2(e, elo, ehi);
-          asm("max.NaN.abs.f32 %0, %0, %1, %2;" : "+f"(mx) : "f"(elo), "f"(ehi));
+        for (int p = 0; p < 4; ++p) {
+          const int pi = 4 * hb + p;  // column pair within the block
+          const uint32_t wd = word_of(w[h][2 * b + hb], p);
+          if (kForm == kFormAmax) {
+            const uint64_t e = fma2(pack2(-rw[h].s, -rw[h].s), bf16x2_to_f32x2(wd), m[h][p]);
+            float elo, ehi;
+            unpack2(e, elo, ehi);
+            asm("max.NaN.abs.f32 %0, %0, %1, %2;" : "+f"(mx) : "f"(elo), "f"(ehi));
+          } else {
+            float mlo, mhi;
+            unpack2(m[h][p], mlo, mhi);
+            const float elo = __fmaf_rn(rw[h].s, bf16_lo(wd), -mlo);
+            const float ehi = __fmaf_rn(rw[h].s, bf16_hi(wd), -mhi);
+            bw[h][pi] = f32x2_to_bf16x2(ehi, elo);
+            if (kForm == kFormAmaxKeep)
+              asm("max.NaN.abs.f32 %0, %0, %1, %2;" : "+f"(mx) : "f"(elo), "f"(ehi));
+          }
         }
+      }
+      if constexpr (kForm == kFormAmaxKeep) {
+        uint8_t *box = stage + (c >> 1) * kR4BoxBytes;
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          *reinterpret_cast<uint4 *>(box + (8 * h + g) * 128 +
+                                     (((4 * (c & 1) + 2 * b + hb) ^ g) << 4)) =
+              make_uint4(bw[h][4 * hb], bw[h][4 * hb + 1], bw[h][4 * hb + 2], bw[h][4 * hb + 3]);
       }
     }
   }
@@ -601,12 +630,16 @@ __device__ __forceinline__ void r4_prime(const R4Maps &tm, R4Ring &rg, int64_t i
 
 // One pass of a warp over its iters row tiles in the order tile_of(i).
 // `resident` tiles at the start of the sequence are already in the ring
-// (the previous pass waited for them).  Returns false if a ring wait gave up
-// (kDevTimeout is raised and the warp's other copies in flight are waited
-// for, bounded).
-template <bool kQuant, typename TileOf>
+// (the previous pass waited for them, and left W_eff there, so the
+// quantisation pass quantises them without a rebuild).  In the amax pass the
+// tiles from position `keep_from` on stay resident for the quantisation
+// pass, which gets their W_eff in the ring.  Returns false if a ring wait
+// gave up (kDevTimeout is raised and the warp's other copies in flight are
+// waited for, bounded).
+template <bool kQuant, bool kKeep, typename TileOf>
 __device__ __forceinline__ bool r4_pass(const R4Maps &tm, R4Ring &rg, int64_t iters,
-                                        int64_t base, int resident, TileOf tile_of,
+                                        int64_t base, int resident, int64_t keep_from,
+                                        TileOf tile_of,
                                         int64_t col0, int k, int n, int64_t tiles_k,
                                         int64_t tk, const float *vc, int lane, float g_enc,
                                         const float *rcp_tab, bool ok, float &mx,
@@ -642,11 +675,30 @@ __device__ __forceinline__ bool r4_pass(const R4Maps &tm, R4Ring &rg, int64_t it
                tile_of(i + kR4Stages), col0, k);
     uint32_t sword = 0;
     if (live) {
-      uint64_t nu[2][4];
-      r4_pairs(rw, nu);
+      uint8_t *stage = rg.ring + st * kR4StageBytes;
       uint32_t out[2][4];
-      sword |= r4_block<kQuant>(w, rw, nu, vc, 0, g_enc, rcp_tab, ok, mx, out);
-      sword |= r4_block<kQuant>(w, rw, nu, vc, 1, g_enc, rcp_tab, ok, mx, out);
+      if (kKeep && kQuant && i < resident) {
+        const uint64_t nu[2][4] = {};
+        sword |= r4_block<kFormQuantEff>(w, rw, nu, vc, 0, g_enc, rcp_tab, ok, mx, out, stage,
+                                         g, c);
+        sword |= r4_block<kFormQuantEff>(w, rw, nu, vc, 1, g_enc, rcp_tab, ok, mx, out, stage,
+                                         g, c);
+      } else {
+        uint64_t nu[2][4];
+        r4_pairs(rw, nu);
+        if (kQuant) {
+          sword |= r4_block<kFormQuant>(w, rw, nu, vc, 0, g_enc, rcp_tab, ok, mx, out, stage,
+                                        g, c);
+          sword |= r4_block<kFormQuant>(w, rw, nu, vc, 1, g_enc, rcp_tab, ok, mx, out, stage,
+                                        g, c);
+        } else if (kKeep && i >= keep_from) {
+          r4_block<kFormAmaxKeep>(w, rw, nu, vc, 0, g_enc, rcp_tab, ok, mx, out, stage, g, c);
+          r4_block<kFormAmaxKeep>(w, rw, nu, vc, 1, g_enc, rcp_tab, ok, mx, out, stage, g, c);
+        } else {
+          r4_block<kFormAmax>(w, rw, nu, vc, 0, g_enc, rcp_tab, ok, mx, out, stage, g, c);
+          r4_block<kFormAmax>(w, rw, nu, vc, 1, g_enc, rcp_tab, ok, mx, out, stage, g, c);
+        }
+      }
       if (kQuant) {
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
@@ -670,7 +722,11 @@ __device__ __forceinline__ bool r4_pass(const R4Maps &tm, R4Ring &rg, int64_t it
 // starting on the two the amax pass left in its ring.  amax_bits[0..2] are
 // zero at the start of the call, and the quantisation pass leaves them so
 // (depart_and_clear).
-constexpr int kR4Amax = 0, kR4Quant = 1, kR4Both = 2;
+// kR4BothKeep is kR4Both with the W_eff hand-over: the amax pass leaves the
+// W_eff of each warp's last two tiles in its ring and the quantisation pass
+// quantises them without a rebuild (worth it when a warp has few tiles; its
+// extra code costs the main loop registers).
+constexpr int kR4Amax = 0, kR4Quant = 1, kR4Both = 2, kR4BothKeep = 3;
 
 template <int kMode>
 __global__ void __launch_bounds__(kR4Threads, 2)
@@ -678,6 +734,8 @@ __global__ void __launch_bounds__(kR4Threads, 2)
                     int k, uint8_t *__restrict__ packed,
                     uint8_t *__restrict__ scales, float *__restrict__ global_scale,
                     uint32_t *amax_bits, unsigned *status) {
+  constexpr bool kBoth = kMode == kR4Both || kMode == kR4BothKeep;
+  constexpr bool kKeep = kMode == kR4BothKeep;
   extern __shared__ uint8_t r4_smem_raw[];
   __shared__ float rcp_tab[128];
   __shared__ int never;  // abort flag of the bounded waits; nothing sets it
@@ -718,8 +776,12 @@ __global__ void __launch_bounds__(kR4Threads, 2)
 
   if (kMode != kR4Quant) {
     float mx = 0.0f;
-    ring_ok = r4_pass<false>(tm, rg, iters, 0, 0, fwd, col0, k, n, tiles_k, tk, vc, lane, 1.0f,
-                             rcp_tab, true, mx, nullptr, nullptr, &never, status);
+    // with the quantisation pass in the same launch, the last two tiles stay
+    // resident with their W_eff
+    const int64_t keep_from =
+        kBoth ? (iters > kR4Stages ? iters - kR4Stages : 0) : iters;
+    ring_ok = r4_pass<false, kKeep>(tm, rg, iters, 0, 0, keep_from, fwd, col0, k, n, tiles_k, tk, vc,
+                             lane, 1.0f, rcp_tab, true, mx, nullptr, nullptr, &never, status);
     // bf16 bits of the largest |e|: a NaN stays a NaN pattern and an
     // infinity the infinity pattern, both at or above 0x7F80
     const uint32_t m = __float_as_uint(mx);
@@ -730,7 +792,7 @@ __global__ void __launch_bounds__(kR4Threads, 2)
   }
   if (kMode == kR4Amax) return;
 
-  if (kMode == kR4Both) {
+  if (kBoth) {
     // grid barrier: release this CTA's maximum, count it in, wait for all
     if (threadIdx.x == 0) {
       int ok_all = 1;
@@ -767,10 +829,10 @@ __global__ void __launch_bounds__(kR4Threads, 2)
   depart_and_clear(amax_bits);
   if (!ring_ok) return;
   float unused = 0.0f;
-  const int resident = kMode == kR4Both ? int(iters < kR4Stages ? iters : kR4Stages) : 0;
-  const int64_t base = kMode == kR4Both ? iters - 1 : 0;
-  r4_pass<true>(tm, rg, iters, base, resident, rev, col0, k, n, tiles_k, tk, vc, lane, g_enc,
-                rcp_tab, ok, unused, packed, scales, &never, status);
+  const int resident = kBoth ? int(iters < kR4Stages ? iters : kR4Stages) : 0;
+  const int64_t base = kBoth ? iters - 1 : 0;
+  r4_pass<true, kKeep>(tm, rg, iters, base, resident, iters, rev, col0, k, n, tiles_k, tk, vc, lane,
+                g_enc, rcp_tab, ok, unused, packed, scales, &never, status);
 }
 
 // Activations for the block-scaled MMA path (reading R9: each token row
@@ -890,7 +952,8 @@ static cudaError_t r4_smem_attr(int device) {
   return e;
 }
 
-// CTAs of the cooperative form that can be resident at once (0 if unknown).
+// CTAs of a cooperative form that can be resident at once (0 if unknown).
+template <int kMode>
 static int64_t r4_both_capacity(const DeviceInfo &dev) {
   static int per_sm[64] = {};
   static std::mutex mu;
@@ -898,13 +961,16 @@ static int64_t r4_both_capacity(const DeviceInfo &dev) {
   if (dev.ordinal < 0 || dev.ordinal >= 64) return 0;
   if (per_sm[dev.ordinal] == 0) {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, recon_r4_kernel<kR4Both>, kR4Threads,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, recon_r4_kernel<kMode>, kR4Threads,
                                                       kR4SmemBytes) != cudaSuccess)
       nb = -1;
     per_sm[dev.ordinal] = nb > 0 ? nb : -1;
   }
   return per_sm[dev.ordinal] > 0 ? int64_t(per_sm[dev.ordinal]) * dev.sms : 0;
 }
+
+// The W_eff hand-over pays while a warp has at most this many row tiles.
+constexpr int64_t kR4KeepMaxTiles = 8;
 
 static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uint16_t *U,
                                     const uint16_t *V, int n, int k,
@@ -918,6 +984,7 @@ static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uin
   cudaError_t e = r4_smem_attr<kR4Amax>(dev.ordinal);
   if (e == cudaSuccess) e = r4_smem_attr<kR4Quant>(dev.ordinal);
   if (e == cudaSuccess) e = r4_smem_attr<kR4Both>(dev.ordinal);
+  if (e == cudaSuccess) e = r4_smem_attr<kR4BothKeep>(dev.ordinal);
   if (e != cudaSuccess) return e;
   const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
   int64_t G = ceil_div(tiles_k * tiles_n, kR4Warps);
@@ -938,7 +1005,15 @@ static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uin
   attr[1].id = cudaLaunchAttributeCooperative;
   attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  if (g <= r4_both_capacity(dev)) {
+  // the most row tiles a warp gets: its tile column's tiles over the
+  // column's (fewest) warps
+  const int64_t most_tiles = ceil_div(tiles_n, G * kR4Warps / tiles_k);
+  if (most_tiles <= kR4KeepMaxTiles && g <= r4_both_capacity<kR4BothKeep>(dev)) {
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4BothKeep>, tm, V, n, k, packed, scales,
+                              gs, amax, status);
+  }
+  if (g <= r4_both_capacity<kR4Both>(dev)) {
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Both>, tm, V, n, k, packed, scales, gs,
                               amax, status);

@@ -243,13 +243,15 @@ def _fused_r4(W0b, s, Ub, Vb):
 
 
 @pytest.mark.parametrize("n,k", [(1, 32), (45, 160), (17, 4128), (300, 1152), (20, 40960),
-                                 (16, 320000)])
+                                 (16, 320000), (7680, 5376)])
 def test_rank4_packed_path_ragged_shapes_bit_exact(n, k):
     """The rank-4 path with V 16-byte aligned on row counts that end inside a
     16-row tile and widths that end inside a 128-column tile column.  At
     k = 320000 there are more tile columns (2500) than warps the GPU holds
     at once, so the amax and quantisation passes run as two launches instead
-    of one cooperative launch."""
+    of one cooperative launch.  [7680, 5376] gives a warp about nine row
+    tiles, which takes the cooperative form without the W_eff hand-over (the
+    smaller shapes take the hand-over)."""
     th = inputs.theta(n, k, 4, seed=n * 7 + k, device=DEV)
     assert th.V.data_ptr() % 16 == 0
     w = aq.Nvfp4Weight.empty(n, k, device=DEV)
