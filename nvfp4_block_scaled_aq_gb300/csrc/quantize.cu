@@ -12,6 +12,7 @@
 // Every fp32 step that decides a stored bit uses an explicitly rounded
 // intrinsic (__fmul_rn, __fdiv_rn, __fmaf_rn) so the compiler cannot fuse
 // or reorder it.
+#include <cstring>
 #include <mutex>
 
 #include "aq_internal.cuh"
@@ -109,21 +110,6 @@ __device__ __forceinline__ uint32_t block_max_u32(uint32_t v) {
     for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
   }
   return v;
-}
-
-__global__ void __launch_bounds__(kThreads)
-    amax_kernel(const uint16_t *__restrict__ W, int64_t count8, uint32_t *amax_bits) {
-  uint32_t m2 = 0;  // two u16 maxima side by side
-  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < count8;
-       i += int64_t(gridDim.x) * blockDim.x) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(W) + i);
-    m2 = __vmaxu2(m2, v.x & 0x7FFF7FFFu);
-    m2 = __vmaxu2(m2, v.y & 0x7FFF7FFFu);
-    m2 = __vmaxu2(m2, v.z & 0x7FFF7FFFu);
-    m2 = __vmaxu2(m2, v.w & 0x7FFF7FFFu);
-  }
-  uint32_t m = block_max_u32(max(m2 & 0xFFFFu, m2 >> 16));
-  if (threadIdx.x == 0) atomicMax(amax_bits, m);
 }
 
 template <int R>
@@ -283,10 +269,11 @@ __device__ __forceinline__ uint32_t quantize_block16(const uint32_t (&bw)[8], fl
   return sf;
 }
 
-// One warp per 16 x 128 tile; lane 4g + c owns rows g and g + 8 of the
-// tile and columns [32c, 32c + 32), i.e. two blocks per row, and writes the
-// one 32-bit scale word of the layout that holds exactly those four scales.
-template <int R, bool kFused>
+// The fused form for ranks and alignments the rank-4 kernel does not serve:
+// one warp per 16 x 128 tile; lane 4g + c owns rows g and g + 8 of the tile
+// and columns [32c, 32c + 32), i.e. two blocks per row, and writes the one
+// 32-bit scale word of the layout that holds exactly those four scales.
+template <int R>
 __global__ void __launch_bounds__(kThreads)
     quantize_kernel(const uint16_t *__restrict__ W, const float *__restrict__ s,
                     const uint16_t *__restrict__ U, const uint16_t *__restrict__ V,
@@ -319,16 +306,7 @@ __global__ void __launch_bounds__(kThreads)
       const int64_t row = tn * kTileRows + 8 * h + g;
       if (row >= n || col >= k) continue;
       uint32_t bw[2][8];  // the row's 32 values as bf16 pairs, per block
-      if (!kFused) {
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 v = __ldg(reinterpret_cast<const uint4 *>(W + row * k + col) + q);
-          bw[q >> 1][4 * (q & 1)] = v.x;
-          bw[q >> 1][4 * (q & 1) + 1] = v.y;
-          bw[q >> 1][4 * (q & 1) + 2] = v.z;
-          bw[q >> 1][4 * (q & 1) + 3] = v.w;
-        }
-      } else {
+      {
         const float srow = __ldg(s + row);
         if (R != 0) load_urow<R>(u, U, row, r);
         const int rr = R >= 0 ? R : r;
@@ -466,17 +444,22 @@ __device__ __forceinline__ void tma_load_1d(void *dst, const CUtensorMap *map, i
       : "memory");
 }
 
+// kPlain: a bf16 weight quantised as it is (no theta bundle): the tile's
+// weights only.
+template <bool kPlain>
 __device__ __forceinline__ void r4_issue(const R4Maps &tm, uint8_t *stage, uint8_t *rows,
                                          uint64_t *bar, int64_t tn, int64_t col0, int k) {
   const bool two = col0 + 64 < k;
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  core::mbar_expect_tx(bar, (two ? kR4StageBytes : kR4BoxBytes) + kR4RowBytes);
+  core::mbar_expect_tx(bar, (two ? kR4StageBytes : kR4BoxBytes) + (kPlain ? 0 : kR4RowBytes));
   core::tma_load_2d(stage, &tm.w0, int(col0 * 2), int(tn * kTileRows), bar);
   if (two)
     core::tma_load_2d(stage + kR4BoxBytes, &tm.w0, int(col0 * 2 + 128), int(tn * kTileRows),
                       bar);
-  tma_load_1d(rows, &tm.u, int(tn * kTileRows * 8), bar);
-  tma_load_1d(rows + kTileRows * 8, &tm.s, int(tn * kTileRows * 4), bar);
+  if (!kPlain) {
+    tma_load_1d(rows, &tm.u, int(tn * kTileRows * 8), bar);
+    tma_load_1d(rows + kTileRows * 8, &tm.s, int(tn * kTileRows * 4), bar);
+  }
 }
 
 __device__ __forceinline__ R4Row r4_row(const uint8_t *rows, int r) {
@@ -618,12 +601,12 @@ struct R4Ring {
 };
 static_assert(kR4Stages == 2, "the resident-tile hand-over assumes two stages");
 
-template <typename TileOf>
+template <bool kPlain, typename TileOf>
 __device__ __forceinline__ void r4_prime(const R4Maps &tm, R4Ring &rg, int64_t iters,
                                          TileOf tile_of, int64_t col0, int k, int lane) {
   if (lane == 0)
     for (int d = 0; d < kR4Stages && d < iters; ++d)
-      r4_issue(tm, rg.ring + d * kR4StageBytes, rg.rows + d * kR4RowStride, &rg.bars[d],
+      r4_issue<kPlain>(tm, rg.ring + d * kR4StageBytes, rg.rows + d * kR4RowStride, &rg.bars[d],
                tile_of(d), col0, k);
   __syncwarp();
 }
@@ -636,14 +619,14 @@ __device__ __forceinline__ void r4_prime(const R4Maps &tm, R4Ring &rg, int64_t i
 // pass, which gets their W_eff in the ring.  Returns false if a ring wait
 // gave up (kDevTimeout is raised and the warp's other copies in flight are
 // waited for, bounded).
-template <bool kQuant, bool kKeep, typename TileOf>
+template <bool kQuant, bool kKeep, bool kPlain, typename TileOf>
 __device__ __forceinline__ bool r4_pass(const R4Maps &tm, R4Ring &rg, int64_t iters,
                                         int64_t base, int resident, int64_t keep_from,
                                         TileOf tile_of,
                                         int64_t col0, int k, int n, int64_t tiles_k,
                                         int64_t tk, const float *vc, int lane, float g_enc,
                                         const float *rcp_tab, bool ok, float &mx,
-                                        uint8_t *__restrict__ packed,
+                                        uint32_t &mbits, uint8_t *__restrict__ packed,
                                         uint8_t *__restrict__ scales, volatile int *never,
                                         unsigned *status) {
   const int g = lane >> 2, c = lane & 3;
@@ -671,13 +654,26 @@ __device__ __forceinline__ bool r4_pass(const R4Maps &tm, R4Ring &rg, int64_t it
                          r4_row(rg.rows + st * kR4RowStride, 8 + g)};
     __syncwarp();
     if (lane == 0 && i + kR4Stages < iters)
-      r4_issue(tm, rg.ring + st * kR4StageBytes, rg.rows + st * kR4RowStride, &rg.bars[st],
+      r4_issue<kPlain>(tm, rg.ring + st * kR4StageBytes, rg.rows + st * kR4RowStride,
+                       &rg.bars[st],
                tile_of(i + kR4Stages), col0, k);
     uint32_t sword = 0;
     if (live) {
       uint8_t *stage = rg.ring + st * kR4StageBytes;
       uint32_t out[2][4];
-      if (kKeep && kQuant && i < resident) {
+      if (kPlain && !kQuant) {
+        // largest magnitude as bf16 bit patterns with the sign cleared (a
+        // NaN or an infinity sorts above every finite value), two per word
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            mbits = __vmaxu2(mbits, w[h][q].x & 0x7FFF7FFFu);
+            mbits = __vmaxu2(mbits, w[h][q].y & 0x7FFF7FFFu);
+            mbits = __vmaxu2(mbits, w[h][q].z & 0x7FFF7FFFu);
+            mbits = __vmaxu2(mbits, w[h][q].w & 0x7FFF7FFFu);
+          }
+      } else if ((kPlain || kKeep) && kQuant && (kPlain || i < resident)) {
         const uint64_t nu[2][4] = {};
         sword |= r4_block<kFormQuantEff>(w, rw, nu, vc, 0, g_enc, rcp_tab, ok, mx, out, stage,
                                          g, c);
@@ -715,7 +711,7 @@ __device__ __forceinline__ bool r4_pass(const R4Maps &tm, R4Ring &rg, int64_t it
 }
 
 // The rank-4 passes.  kR4Amax: max |e| over the tensor into amax_bits[0] as
-// bf16 bits (like amax_kernel).  kR4Quant: the quantisation pass.  kR4Both:
+// bf16 bits with the sign cleared.  kR4Quant: the quantisation pass.  kR4Both:
 // both in one cooperative launch -- every CTA folds its maximum into
 // amax_bits[0], arrives on amax_bits[1] and waits (bounded) until all CTAs
 // have; the quantisation pass then walks each warp's tiles backwards,
@@ -728,7 +724,10 @@ __device__ __forceinline__ bool r4_pass(const R4Maps &tm, R4Ring &rg, int64_t it
 // extra code costs the main loop registers).
 constexpr int kR4Amax = 0, kR4Quant = 1, kR4Both = 2, kR4BothKeep = 3;
 
-template <int kMode>
+// kPlain: the same passes over a bf16 weight W (tm.w0) quantised as it is,
+// for aq_quantize_nvfp4: the amax pass takes the largest bf16 magnitude
+// straight from the ring, the quantisation pass quantises the ring's bytes.
+template <int kMode, bool kPlain = false>
 __global__ void __launch_bounds__(kR4Threads, 2)
     recon_r4_kernel(const __grid_constant__ R4Maps tm, const uint16_t *__restrict__ V, int n,
                     int k, uint8_t *__restrict__ packed,
@@ -766,10 +765,10 @@ __global__ void __launch_bounds__(kR4Threads, 2)
   pdl_launch_dependents();
   pdl_wait();
   if (kMode == kR4Quant)
-    r4_prime(tm, rg, iters, rev, col0, k, lane);
+    r4_prime<kPlain>(tm, rg, iters, rev, col0, k, lane);
   else
-    r4_prime(tm, rg, iters, fwd, col0, k, lane);
-  stage_vt(V, col0, k, lane, vt);
+    r4_prime<kPlain>(tm, rg, iters, fwd, col0, k, lane);
+  if (!kPlain) stage_vt(V, col0, k, lane, vt);
   __syncthreads();
   const float *vc = vt + c * kVtPitch;
   bool ring_ok = true;
@@ -780,13 +779,16 @@ __global__ void __launch_bounds__(kR4Threads, 2)
     // resident with their W_eff
     const int64_t keep_from =
         kBoth ? (iters > kR4Stages ? iters - kR4Stages : 0) : iters;
-    ring_ok = r4_pass<false, kKeep>(tm, rg, iters, 0, 0, keep_from, fwd, col0, k, n, tiles_k, tk, vc,
-                             lane, 1.0f, rcp_tab, true, mx, nullptr, nullptr, &never, status);
+    uint32_t mbits = 0;
+    ring_ok = r4_pass<false, kKeep, kPlain>(tm, rg, iters, 0, 0, keep_from, fwd, col0, k, n,
+                                            tiles_k, tk, vc, lane, 1.0f, rcp_tab, true, mx,
+                                            mbits, nullptr, nullptr, &never, status);
     // bf16 bits of the largest |e|: a NaN stays a NaN pattern and an
     // infinity the infinity pattern, both at or above 0x7F80
     const uint32_t m = __float_as_uint(mx);
-    uint32_t mb = m >= 0x7F800000u ? (m >> 16) | (m > 0x7F800000u ? 0x40u : 0u)
-                                   : uint32_t(f32_to_bf16_rn(mx));
+    uint32_t mb = kPlain ? max(mbits & 0xFFFFu, mbits >> 16)
+                  : m >= 0x7F800000u ? (m >> 16) | (m > 0x7F800000u ? 0x40u : 0u)
+                                     : uint32_t(f32_to_bf16_rn(mx));
     mb = block_max_u32<kR4Threads>(mb);
     if (threadIdx.x == 0) atomicMax(amax_bits, mb);
   }
@@ -831,8 +833,10 @@ __global__ void __launch_bounds__(kR4Threads, 2)
   float unused = 0.0f;
   const int resident = kBoth ? int(iters < kR4Stages ? iters : kR4Stages) : 0;
   const int64_t base = kBoth ? iters - 1 : 0;
-  r4_pass<true, kKeep>(tm, rg, iters, base, resident, iters, rev, col0, k, n, tiles_k, tk, vc, lane,
-                g_enc, rcp_tab, ok, unused, packed, scales, &never, status);
+  uint32_t unused_bits = 0;
+  r4_pass<true, kKeep, kPlain>(tm, rg, iters, base, resident, iters, rev, col0, k, n, tiles_k,
+                               tk, vc, lane, g_enc, rcp_tab, ok, unused, unused_bits, packed,
+                               scales, &never, status);
 }
 
 // Activations for the block-scaled MMA path (reading R9: each token row
@@ -916,44 +920,41 @@ cudaError_t launch_reconstruct(const uint16_t *W0, const float *s, const uint16_
   return cudaGetLastError();
 }
 
-template <int R, bool kFused>
+// The per-element fused form (ranks other than 4, or U, s or V not 16-byte
+// aligned): the amax pass, then the quantisation pass, both grid-stride.
+template <int R>
 static void quantize_pass(const uint16_t *W, const float *s, const uint16_t *U,
                           const uint16_t *V, int r, int n, int k,
                           const aq_nvfp4_weight &out, uint32_t *amax, const DeviceInfo &dev,
                           cudaStream_t st) {
   const int cap = dev.sms * 8;
-  if (kFused) {
-    const int g = grid_for(int64_t(n) * (k / 8), kThreads, cap);
-    amax_fused_kernel<R><<<g, kThreads, 0, st>>>(W, s, U, V, n, k, r, amax);
-  } else {
-    const int g = grid_for(int64_t(n) * k / 8, kThreads, cap);
-    amax_kernel<<<g, kThreads, 0, st>>>(W, int64_t(n) * k / 8, amax);
-  }
+  const int ga = grid_for(int64_t(n) * (k / 8), kThreads, cap);
+  amax_fused_kernel<R><<<ga, kThreads, 0, st>>>(W, s, U, V, n, k, r, amax);
   const int64_t tiles = ceil_div(n, kTileRows) * ceil_div(k, kTileCols);
   const int g = grid_for(tiles, kThreads / 32, cap);
-  quantize_kernel<R, kFused><<<g, kThreads, 0, st>>>(W, s, U, V, n, k, r, out.packed,
-                                                     out.scales, out.global_scale, amax,
-                                                     dev.status);
+  quantize_kernel<R><<<g, kThreads, 0, st>>>(W, s, U, V, n, k, r, out.packed, out.scales,
+                                             out.global_scale, amax, dev.status);
 }
 
 // Rank 4: two CTAs per SM (fewer for a small tensor), so that every SM
 // carries the same number of warps; every tile column needs a warp, and
 // when that takes more CTAs than fit on the GPU at once the two passes run
 // as two launches, else as one cooperative launch (kR4Both).
-template <int kMode>
+template <int kMode, bool kPlain = false>
 static cudaError_t r4_smem_attr(int device) {
   static bool done[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(
-      recon_r4_kernel<kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize, kR4SmemBytes);
+  const cudaError_t e = cudaFuncSetAttribute(recon_r4_kernel<kMode, kPlain>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kR4SmemBytes);
   if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
   return e;
 }
 
 // CTAs of a cooperative form that can be resident at once (0 if unknown).
-template <int kMode>
+template <int kMode, bool kPlain = false>
 static int64_t r4_both_capacity(const DeviceInfo &dev) {
   static int per_sm[64] = {};
   static std::mutex mu;
@@ -961,8 +962,8 @@ static int64_t r4_both_capacity(const DeviceInfo &dev) {
   if (dev.ordinal < 0 || dev.ordinal >= 64) return 0;
   if (per_sm[dev.ordinal] == 0) {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, recon_r4_kernel<kMode>, kR4Threads,
-                                                      kR4SmemBytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, recon_r4_kernel<kMode, kPlain>,
+                                                      kR4Threads, kR4SmemBytes) != cudaSuccess)
       nb = -1;
     per_sm[dev.ordinal] = nb > 0 ? nb : -1;
   }
@@ -972,19 +973,16 @@ static int64_t r4_both_capacity(const DeviceInfo &dev) {
 // The W_eff hand-over pays while a warp has at most this many row tiles.
 constexpr int64_t kR4KeepMaxTiles = 8;
 
-static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uint16_t *U,
-                                    const uint16_t *V, int n, int k,
-                                    const aq_nvfp4_weight &out, uint32_t *amax,
-                                    const DeviceInfo &dev, cudaStream_t st) {
-  R4Maps tm;
-  if (!core::encode_bf16_rows_map(W, n, k, kTileRows, &tm.w0) ||
-      !core::encode_bytes_1d(U, uint64_t(n) * 8, kTileRows * 8, &tm.u) ||
-      !core::encode_bytes_1d(s, uint64_t(n) * 4, kTileRows * 4, &tm.s))
-    return cudaErrorInvalidValue;
-  cudaError_t e = r4_smem_attr<kR4Amax>(dev.ordinal);
-  if (e == cudaSuccess) e = r4_smem_attr<kR4Quant>(dev.ordinal);
-  if (e == cudaSuccess) e = r4_smem_attr<kR4Both>(dev.ordinal);
-  if (e == cudaSuccess) e = r4_smem_attr<kR4BothKeep>(dev.ordinal);
+// Both passes over a weight of [n, k]: kPlain for a bf16 W in tm.w0, else
+// the rank-4 theta bundle (tm.w0 = W0, tm.u, tm.s, V).
+template <bool kPlain>
+static cudaError_t r4_launch(const R4Maps &tm, const uint16_t *V, int n, int k,
+                             const aq_nvfp4_weight &out, uint32_t *amax, const DeviceInfo &dev,
+                             cudaStream_t st) {
+  cudaError_t e = r4_smem_attr<kR4Amax, kPlain>(dev.ordinal);
+  if (e == cudaSuccess) e = r4_smem_attr<kR4Quant, kPlain>(dev.ordinal);
+  if (e == cudaSuccess) e = r4_smem_attr<kR4Both, kPlain>(dev.ordinal);
+  if (e == cudaSuccess && !kPlain) e = r4_smem_attr<kR4BothKeep>(dev.ordinal);
   if (e != cudaSuccess) return e;
   const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
   int64_t G = ceil_div(tiles_k * tiles_n, kR4Warps);
@@ -1008,23 +1006,45 @@ static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uin
   // the most row tiles a warp gets: its tile column's tiles over the
   // column's (fewest) warps
   const int64_t most_tiles = ceil_div(tiles_n, G * kR4Warps / tiles_k);
-  if (most_tiles <= kR4KeepMaxTiles && g <= r4_both_capacity<kR4BothKeep>(dev)) {
+  if (!kPlain && most_tiles <= kR4KeepMaxTiles && g <= r4_both_capacity<kR4BothKeep>(dev)) {
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4BothKeep>, tm, V, n, k, packed, scales,
                               gs, amax, status);
   }
-  if (g <= r4_both_capacity<kR4Both>(dev)) {
+  if (g <= r4_both_capacity<kR4Both, kPlain>(dev)) {
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Both>, tm, V, n, k, packed, scales, gs,
-                              amax, status);
+    return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Both, kPlain>, tm, V, n, k, packed,
+                              scales, gs, amax, status);
   }
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Amax>, tm, V, n, k,
+  e = cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Amax, kPlain>, tm, V, n, k,
                          static_cast<uint8_t *>(nullptr), static_cast<uint8_t *>(nullptr),
                          static_cast<float *>(nullptr), amax, status);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Quant>, tm, V, n, k, packed, scales, gs,
-                            amax, status);
+  return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4Quant, kPlain>, tm, V, n, k, packed,
+                            scales, gs, amax, status);
+}
+
+static cudaError_t quantize_pass_r4(const uint16_t *W, const float *s, const uint16_t *U,
+                                    const uint16_t *V, int n, int k,
+                                    const aq_nvfp4_weight &out, uint32_t *amax,
+                                    const DeviceInfo &dev, cudaStream_t st) {
+  R4Maps tm;
+  if (!core::encode_bf16_rows_map(W, n, k, kTileRows, &tm.w0) ||
+      !core::encode_bytes_1d(U, uint64_t(n) * 8, kTileRows * 8, &tm.u) ||
+      !core::encode_bytes_1d(s, uint64_t(n) * 4, kTileRows * 4, &tm.s))
+    return cudaErrorInvalidValue;
+  return r4_launch<false>(tm, V, n, k, out, amax, dev, st);
+}
+
+// A bf16 weight quantised as it is, through the same passes.
+static cudaError_t quantize_pass_plain(const uint16_t *W, int n, int k,
+                                       const aq_nvfp4_weight &out, uint32_t *amax,
+                                       const DeviceInfo &dev, cudaStream_t st) {
+  R4Maps tm;
+  memset(&tm, 0, sizeof(tm));
+  if (!core::encode_bf16_rows_map(W, n, k, kTileRows, &tm.w0)) return cudaErrorInvalidValue;
+  return r4_launch<true>(tm, nullptr, n, k, out, amax, dev, st);
 }
 
 cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U,
@@ -1035,16 +1055,16 @@ cudaError_t launch_quantize(const uint16_t *W, const float *s, const uint16_t *U
   // zero again when the quantisation pass is done
   uint32_t *amax = static_cast<uint32_t *>(ws);
   if (!fused)
-    quantize_pass<0, false>(W, s, U, V, 0, n, k, out, amax, dev, st);
+    return quantize_pass_plain(W, n, k, out, amax, dev, st);
   else if (r == 4 && ((reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(U) |
                         reinterpret_cast<uintptr_t>(s)) & 15u) == 0)
     return quantize_pass_r4(W, s, U, V, n, k, out, amax, dev, st);
   else if (r == 0)
-    quantize_pass<0, true>(W, s, U, V, r, n, k, out, amax, dev, st);
+    quantize_pass<0>(W, s, U, V, r, n, k, out, amax, dev, st);
   else if (r == 4 && (reinterpret_cast<uintptr_t>(V) & 7u) == 0)
-    quantize_pass<4, true>(W, s, U, V, r, n, k, out, amax, dev, st);
+    quantize_pass<4>(W, s, U, V, r, n, k, out, amax, dev, st);
   else
-    quantize_pass<-1, true>(W, s, U, V, r, n, k, out, amax, dev, st);
+    quantize_pass<-1>(W, s, U, V, r, n, k, out, amax, dev, st);
   return cudaGetLastError();
 }
 
