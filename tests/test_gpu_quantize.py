@@ -104,8 +104,11 @@ def test_quantize_adversarial(name):
 
 
 @pytest.mark.parametrize("n,k", [(1, 32), (37, 96), (16, 128), (5, 1184), (100, 2048),
-                                 (1152, 6912)])
+                                 (1152, 6912), (16, 320000)])
 def test_quantize_ragged_and_edge_shapes(n, k):
+    """Plain quantisation on row counts and widths that end inside a tile;
+    at k = 320000 (2500 tile columns, more than the warps the GPU holds at
+    once) the amax and quantisation passes run as two launches."""
     W = inputs.weight(n, k, seed=n * 7 + k, device=DEV)
     w = quantize_gpu(W)
     assert_quantized_equal(w, bits(W))
