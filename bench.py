@@ -46,9 +46,9 @@ NCU_TRAFFIC = {
     # weight of the layer can still sit in L2 from an earlier step), m = 1,
     # one-token kernel form, captured without cache flushing so the L2
     # prefetch of the next projection counts where it is issued: reads
-    # 19,524,096 + 15,062,016 + 143,823,616 + 67,985,664, writes 223,744 +
-    # 86,016 + 469,504 + 228,352 (the committed ncu summary of that capture)
-    ("gemma4-31b-shaped decode-step weight stream", 1, "a32985606f8cc6865ecca4601cbd5245b8dbc79f"): 247403008,
+    # 19,480,320 + 15,461,888 + 144,582,656 + 67,476,736, writes 227,328 +
+    # 102,912 + 492,032 + 238,848 (the committed ncu summary of that capture)
+    ("gemma4-31b-shaped decode-step weight stream", 1, "9615d4ee255ae3c2bd9bdb6ff4c8ba8b51741a51"): 248062720,
 }
 
 

@@ -322,12 +322,19 @@ GemvPlan plan_gemv(int n, int k, const DeviceInfo &dev, int rg) {
   // Of the grids whose longest range is as short as two CTAs per SM allow,
   // the smallest: every range then has that length (or one unit less), so
   // no CTA idles while others finish an extra unit, and fewer CTAs share
-  // each split row block.  The grid depends only on (n, k) and the SM
-  // count, never on m.
+  // each split row block.  A range is never shorter than an eighth of a
+  // row block's units, so at most about eight CTAs share one row block:
+  // small projections with long rows would otherwise spread a row block over
+  // dozens of one-unit CTAs and spend their time in the split-K reduction
+  // (measured on the 1B down [1152, 6912]: 9.1 us per call with 27
+  // contributors, 6.4 us with 7; the ~31B shapes' ranges are longer than
+  // that already).  The grid depends only on (n, k) and the SM count, never
+  // on m.
   int64_t g = int64_t(dev.sms) * (rg == 8 ? Geo<8>::kCtasPerSm : Geo<16>::kCtasPerSm);
   if (g > p.total) g = p.total;
   if (g < 1) g = 1;
-  const int64_t longest = (p.total + g - 1) / g;
+  int64_t longest = (p.total + g - 1) / g;
+  if (longest < (p.units + 7) / 8) longest = (p.units + 7) / 8;
   g = (p.total + longest - 1) / longest;
   p.grid = int(g);
   int worst = 1;
