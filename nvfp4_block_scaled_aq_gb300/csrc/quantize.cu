@@ -418,18 +418,30 @@ struct R4Row {
 constexpr int kR4Stages = 2;
 constexpr int kR4BoxBytes = kTileRows * 128;    // one 16 x 64 box
 constexpr int kR4StageBytes = 2 * kR4BoxBytes;  // one row tile
-constexpr int kR4Warps = 8;  // per CTA; two CTAs (16 warps, 128 registers each) per SM
-// (ten-warp CTAs at 96 registers measured slower: 219 against 206 us on the
-// ~31B gate+up)
-constexpr int kR4Threads = kR4Warps * 32;
 constexpr int kR4RowBytes = kTileRows * 8 + kTileRows * 4;  // U rows, then s
 constexpr int kR4RowStride = 256;  // side buffers 128-byte aligned for the TMA
-constexpr int kR4RingBytes = kR4Warps * kR4Stages * kR4StageBytes;
-constexpr int kR4RowsOffset = kR4RingBytes + kR4Warps * kVtFloats * 4;
-constexpr int kR4BarsOffset = kR4RowsOffset + kR4Warps * kR4Stages * kR4RowStride;
-constexpr int kR4SmemBytes = 1024 + kR4BarsOffset + kR4Warps * kR4Stages * 8;
 
-static_assert(kR4RowsOffset % 128 == 0, "TMA side buffers must be 128-byte aligned");
+// A CTA of kWarps warps: the warps' rings, then their V tiles, their side
+// buffers and their barriers.  Eight warps run as two CTAs per SM, sixteen
+// as one; either way an SM holds 16 warps of up to 128 registers.  The
+// rank-4 two-pass form without the hand-over runs sixteen (202 against
+// 206 us on the ~31B gate+up, where two 8-warp CTAs ended between 185 and
+// 204 us but every SM between 198.5 and 203); the other forms run eight, which is as fast on the ~31B
+// plain quantisation and faster on the 1B shapes (16.7 against 17.5 us on
+// the fused 1B down).  Ten-warp CTAs at 96 registers measured slower (219
+// against 206 us).
+constexpr int kR4Warps = 8, kR4WideWarps = 16;
+template <int kWarps>
+struct R4Geo {
+  static constexpr int kThreads = kWarps * 32;
+  static constexpr int kCtasPerSm = 16 / kWarps;
+  static constexpr int kRingBytes = kWarps * kR4Stages * kR4StageBytes;
+  static constexpr int kRowsOffset = kRingBytes + kWarps * kVtFloats * 4;
+  static constexpr int kBarsOffset = kRowsOffset + kWarps * kR4Stages * kR4RowStride;
+  static constexpr int kSmemBytes = 1024 + kBarsOffset + kWarps * kR4Stages * 8;
+  static_assert(kRowsOffset % 128 == 0, "TMA side buffers must be 128-byte aligned");
+  static_assert(kSmemBytes <= 227 * 1024, "one CTA's shared memory");
+};
 
 struct R4Maps {
   CUtensorMap w0, u, s;
@@ -727,8 +739,8 @@ constexpr int kR4Amax = 0, kR4Quant = 1, kR4Both = 2, kR4BothKeep = 3;
 // kPlain: the same passes over a bf16 weight W (tm.w0) quantised as it is,
 // for aq_quantize_nvfp4: the amax pass takes the largest bf16 magnitude
 // straight from the ring, the quantisation pass quantises the ring's bytes.
-template <int kMode, bool kPlain = false>
-__global__ void __launch_bounds__(kR4Threads, 2)
+template <int kMode, bool kPlain = false, int kWarps = kR4Warps>
+__global__ void __launch_bounds__(R4Geo<kWarps>::kThreads, R4Geo<kWarps>::kCtasPerSm)
     recon_r4_kernel(const __grid_constant__ R4Maps tm, const uint16_t *__restrict__ V, int n,
                     int k, uint8_t *__restrict__ packed,
                     uint8_t *__restrict__ scales, float *__restrict__ global_scale,
@@ -743,11 +755,12 @@ __global__ void __launch_bounds__(kR4Threads, 2)
       (reinterpret_cast<uintptr_t>(r4_smem_raw) + 1023) & ~uintptr_t(1023));
   const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31, c = lane & 3;
   R4Ring rg{smem + wi * kR4Stages * kR4StageBytes,
-            smem + kR4RowsOffset + wi * kR4Stages * kR4RowStride,
-            reinterpret_cast<uint64_t *>(smem + kR4BarsOffset) + wi * kR4Stages, 0u};
-  float *vt = reinterpret_cast<float *>(smem + kR4RingBytes) + wi * kVtFloats;
+            smem + R4Geo<kWarps>::kRowsOffset + wi * kR4Stages * kR4RowStride,
+            reinterpret_cast<uint64_t *>(smem + R4Geo<kWarps>::kBarsOffset) + wi * kR4Stages,
+            0u};
+  float *vt = reinterpret_cast<float *>(smem + R4Geo<kWarps>::kRingBytes) + wi * kVtFloats;
   const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
-  const int64_t nw = int64_t(gridDim.x) * kR4Warps, w = int64_t(blockIdx.x) * kR4Warps + wi;
+  const int64_t nw = int64_t(gridDim.x) * kWarps, w = int64_t(blockIdx.x) * kWarps + wi;
   const int64_t tk = w % tiles_k, col0 = tk * kTileCols, tn0 = w / tiles_k;
   const int64_t rows_in_flight = nw / tiles_k + (tk < nw % tiles_k ? 1 : 0);
   const int64_t iters = tn0 < tiles_n ? ceil_div(tiles_n - tn0, rows_in_flight) : 0;
@@ -789,7 +802,7 @@ __global__ void __launch_bounds__(kR4Threads, 2)
     uint32_t mb = kPlain ? max(mbits & 0xFFFFu, mbits >> 16)
                   : m >= 0x7F800000u ? (m >> 16) | (m > 0x7F800000u ? 0x40u : 0u)
                                      : uint32_t(f32_to_bf16_rn(mx));
-    mb = block_max_u32<kR4Threads>(mb);
+    mb = block_max_u32<R4Geo<kWarps>::kThreads>(mb);
     if (threadIdx.x == 0) atomicMax(amax_bits, mb);
   }
   if (kMode == kR4Amax) return;
@@ -936,25 +949,25 @@ static void quantize_pass(const uint16_t *W, const float *s, const uint16_t *U,
                                              out.global_scale, amax, dev.status);
 }
 
-// Rank 4: two CTAs per SM (fewer for a small tensor), so that every SM
+// Rank 4: 16 warps per SM (fewer for a small tensor), so that every SM
 // carries the same number of warps; every tile column needs a warp, and
 // when that takes more CTAs than fit on the GPU at once the two passes run
 // as two launches, else as one cooperative launch (kR4Both).
-template <int kMode, bool kPlain = false>
+template <int kMode, bool kPlain = false, int kWarps = kR4Warps>
 static cudaError_t r4_smem_attr(int device) {
   static bool done[64] = {};
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
   if (device >= 0 && device < 64 && done[device]) return cudaSuccess;
-  const cudaError_t e = cudaFuncSetAttribute(recon_r4_kernel<kMode, kPlain>,
+  const cudaError_t e = cudaFuncSetAttribute(recon_r4_kernel<kMode, kPlain, kWarps>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kR4SmemBytes);
+                                             R4Geo<kWarps>::kSmemBytes);
   if (e == cudaSuccess && device >= 0 && device < 64) done[device] = true;
   return e;
 }
 
 // CTAs of a cooperative form that can be resident at once (0 if unknown).
-template <int kMode, bool kPlain = false>
+template <int kMode, bool kPlain = false, int kWarps = kR4Warps>
 static int64_t r4_both_capacity(const DeviceInfo &dev) {
   static int per_sm[64] = {};
   static std::mutex mu;
@@ -962,8 +975,9 @@ static int64_t r4_both_capacity(const DeviceInfo &dev) {
   if (dev.ordinal < 0 || dev.ordinal >= 64) return 0;
   if (per_sm[dev.ordinal] == 0) {
     int nb = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, recon_r4_kernel<kMode, kPlain>,
-                                                      kR4Threads, kR4SmemBytes) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &nb, recon_r4_kernel<kMode, kPlain, kWarps>, R4Geo<kWarps>::kThreads,
+            R4Geo<kWarps>::kSmemBytes) != cudaSuccess)
       nb = -1;
     per_sm[dev.ordinal] = nb > 0 ? nb : -1;
   }
@@ -972,6 +986,15 @@ static int64_t r4_both_capacity(const DeviceInfo &dev) {
 
 // The W_eff hand-over pays while a warp has at most this many row tiles.
 constexpr int64_t kR4KeepMaxTiles = 8;
+
+// CTAs of `warps` warps for a weight of tiles_n x tiles_k row tiles: one
+// tile per warp up to 16 warps per SM, and at least one warp per tile column.
+static int64_t r4_grid(int64_t tiles_n, int64_t tiles_k, int warps, const DeviceInfo &dev) {
+  int64_t G = ceil_div(tiles_k * tiles_n, warps);
+  if (G > int64_t(dev.sms) * (16 / warps)) G = int64_t(dev.sms) * (16 / warps);
+  if (G < ceil_div(tiles_k, warps)) G = ceil_div(tiles_k, warps);
+  return G;
+}
 
 // Both passes over a weight of [n, k]: kPlain for a bf16 W in tm.w0, else
 // the rank-4 theta bundle (tm.w0 = W0, tm.u, tm.s, V).
@@ -983,19 +1006,18 @@ static cudaError_t r4_launch(const R4Maps &tm, const uint16_t *V, int n, int k,
   if (e == cudaSuccess) e = r4_smem_attr<kR4Quant, kPlain>(dev.ordinal);
   if (e == cudaSuccess) e = r4_smem_attr<kR4Both, kPlain>(dev.ordinal);
   if (e == cudaSuccess && !kPlain) e = r4_smem_attr<kR4BothKeep>(dev.ordinal);
+  if (e == cudaSuccess && !kPlain) e = r4_smem_attr<kR4Both, false, kR4WideWarps>(dev.ordinal);
   if (e != cudaSuccess) return e;
   const int64_t tiles_k = ceil_div(k, kTileCols), tiles_n = ceil_div(n, kTileRows);
-  int64_t G = ceil_div(tiles_k * tiles_n, kR4Warps);
-  if (G > int64_t(dev.sms) * 2) G = int64_t(dev.sms) * 2;
-  if (G < ceil_div(tiles_k, kR4Warps)) G = ceil_div(tiles_k, kR4Warps);
+  const int64_t G = r4_grid(tiles_n, tiles_k, kR4Warps, dev);
   const int g = int(G);
   uint8_t *packed = out.packed, *scales = out.scales;
   float *gs = out.global_scale;
   unsigned *status = dev.status;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g);
-  cfg.blockDim = dim3(kR4Threads);
-  cfg.dynamicSmemBytes = kR4SmemBytes;
+  cfg.blockDim = dim3(R4Geo<kR4Warps>::kThreads);
+  cfg.dynamicSmemBytes = R4Geo<kR4Warps>::kSmemBytes;
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1010,6 +1032,18 @@ static cudaError_t r4_launch(const R4Maps &tm, const uint16_t *V, int n, int k,
     cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, recon_r4_kernel<kR4BothKeep>, tm, V, n, k, packed, scales,
                               gs, amax, status);
+  }
+  if (!kPlain) {
+    const int64_t gw = r4_grid(tiles_n, tiles_k, kR4WideWarps, dev);
+    if (gw <= r4_both_capacity<kR4Both, false, kR4WideWarps>(dev)) {
+      cudaLaunchConfig_t wide = cfg;
+      wide.gridDim = dim3(unsigned(gw));
+      wide.blockDim = dim3(R4Geo<kR4WideWarps>::kThreads);
+      wide.dynamicSmemBytes = R4Geo<kR4WideWarps>::kSmemBytes;
+      wide.numAttrs = 2;
+      return cudaLaunchKernelEx(&wide, recon_r4_kernel<kR4Both, false, kR4WideWarps>, tm, V, n,
+                                k, packed, scales, gs, amax, status);
+    }
   }
   if (g <= r4_both_capacity<kR4Both, kPlain>(dev)) {
     cfg.numAttrs = 2;
