@@ -252,9 +252,10 @@ def test_rank4_packed_path_ragged_shapes_bit_exact(n, k):
     16-row tile and widths that end inside a 128-column tile column.  At
     k = 320000 there are more tile columns (2500) than warps the GPU holds
     at once, so the amax and quantisation passes run as two launches instead
-    of one cooperative launch.  [7680, 5376] gives a warp about nine row
-    tiles, which takes the cooperative form without the W_eff hand-over (the
-    smaller shapes take the hand-over)."""
+    of one cooperative launch.  [7680, 5376] gives an 8-warp CTA's warp
+    about nine row tiles, which takes the cooperative form without the W_eff
+    hand-over, launched as one 16-warp CTA per SM (the smaller shapes take
+    the hand-over with two 8-warp CTAs per SM)."""
     th = inputs.theta(n, k, 4, seed=n * 7 + k, device=DEV)
     assert th.V.data_ptr() % 16 == 0
     w = aq.Nvfp4Weight.empty(n, k, device=DEV)
