@@ -266,6 +266,34 @@ def test_rank4_packed_path_ragged_shapes_bit_exact(n, k):
     assert aq.poll_device_status() == aq.OK
 
 
+def test_rank4_31b_gate_up_full_size_sampled_rows_bit_exact():
+    """The ~31B fused gate+up theta bundle [43008, 5376] at rank 4, in the
+    launch form `bench.py --load-time` times (one cooperative launch of
+    16-warp CTAs, one per SM).  The oracle rebuilds the whole W_eff for the
+    per-tensor amax.  g_dec must match bit for bit.  So must the packed
+    bytes and the device-layout scale bytes of 256 seeded rows; each
+    (row, block) scale is located through the oracle's own layout
+    function."""
+    n, k = 43008, 5376
+    th = inputs.theta(n, k, 4, seed=4300, device=DEV)
+    w = aq.Nvfp4Weight.empty(n, k, device=DEV)
+    ws = torch.zeros(aq.quantize_workspace_bytes(), dtype=torch.uint8, device=DEV)
+    aq.reconstruct_quantize(th.W0, th.s, th.U, th.V, w, ws)
+    assert aq.poll_device_status() == aq.OK
+    W_eff = oracle.reconstruct(bits(th.W0), th.s.cpu().numpy(), bits(th.U), bits(th.V))
+    ge, gd = oracle.global_scales(oracle.amax(W_eff))
+    rows = np.sort(np.random.default_rng(4300).choice(n, 256, replace=False))
+    packed, scales = oracle.quantize_rows(W_eff[rows], ge)
+    gp, gs, ggd = weight_bytes(w)
+    assert np.float32(ggd) == np.float32(gd), (ggd, gd)
+    bad = np.argwhere(gp[rows] != packed)
+    assert bad.size == 0, "packed differs at sampled (row index, byte) %s" % bad[:5].tolist()
+    for i, r in enumerate(rows):
+        got = np.array([gs[oracle.scale_layout_offset(int(r), b, k)] for b in range(k // 16)],
+                       np.uint8)
+        assert np.array_equal(got, scales[i]), "scales of row %d differ" % r
+
+
 def test_rank4_zero_signs_and_exact_cancellation_bit_exact():
     """AttnQuant docs, landing page, "How it works": W_eff = s*W0 + U*V^T,
     with the rank term zero handled as s*W0 alone.  Rows built so that
