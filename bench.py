@@ -103,6 +103,17 @@ def algorithmic_bytes(shapes, layers, m):
     return per_layer * layers
 
 
+def load_time_bytes(n, k, r, fused):
+    """Algorithmic bytes of one load-time call on an [n, k] weight: the bf16
+    weight (W0 for the fused form) read once, the packed nibbles, one E4M3
+    scale per 16 elements and the fp32 g_dec written; the fused form also
+    reads s (fp32 per row) and U, V (bf16, rank r)."""
+    byts = n * k * 2 + n * k // 2 + n * k // 16 + 4
+    if fused:
+        byts += 4 * n + 2 * (n + k) * r
+    return byts
+
+
 def weight_bytes(shapes, layers):
     return sum(n * k // 2 + n * k // 16 for n, k in shapes) * layers
 
@@ -851,9 +862,7 @@ def run_load_time(a, dist):
                 e1.record(stream)
             torch.cuda.synchronize()
             secs = e0.elapsed_time(e1) / 1e3 / reps
-            byts = n * k * 2 + n * k // 2 + n * k // 16 + 4
-            if form == "reconstruct_quantize":
-                byts += 4 * n + 2 * (n + k) * r
+            byts = load_time_bytes(n, k, r, form == "reconstruct_quantize")
             res[form] = {"us_per_call": round(secs * 1e6, 2), "GBps": round(byts / secs / 1e9, 1),
                          "algorithmic_bytes": byts}
         st = aq.poll_device_status()
@@ -863,11 +872,14 @@ def run_load_time(a, dist):
         del thetas
     peak, src = load_peaks()
     if dist.rank == 0:
-        best = max(v["GBps"] for row in rows for k2, v in row.items() if isinstance(v, dict))
+        # the headline: the fused call on the largest shape (the ~31B gate+up)
+        head = max(rows, key=lambda row: row["shape"][0] * row["shape"][1])
         print(json.dumps({"metric": "load-time reconstruct + NVFP4 quantise, GB/s of algorithmic bytes",
-                          "value": best, "unit": "GB/s", "n_gpus": dist.world, "higher_is_better": True,
+                          "value": head["reconstruct_quantize"]["GBps"], "unit": "GB/s",
+                          "n_gpus": dist.world, "higher_is_better": True,
                           "data": "synthetic (seeded theta bundles, N(0, 0.02^2) W0)",
                           "config": {"workload": "load-time kernels on the 1B MLP and ~31B gate+up shapes",
+                                     "value_of": "%s fused reconstruct + quantise" % head["name"],
                                      "l2": "inputs rotated over copies exceeding 256 MB"},
                           "hbm_peak_gbs": peak, "hbm_peak_source": src, "shapes": rows}), flush=True)
 
